@@ -1,0 +1,463 @@
+#!/usr/bin/env python
+"""Benchmark of the streaming chunk-attention hot path on one GB300 (replicas for N > 1).
+
+One step = one streamed chunk of the Wan-1.3B-shaped 480p stream at steady state (full sink +
+window): the motion magnitude of the chunk's video frames, then for each of 2 denoise steps and
+each of 30 layers, sdv2_rope_append_kv followed by sdv2_chunk_attention.
+
+value   : chunk-attention TFLOP/s over the whole step (4*H*D*Nq*Nkv flops per attention call,
+          divided by the step's wall time on the device; inputs resident in HBM).
+e2e     : the same metric when every call's q, k, v come from pinned host buffers and every
+          attention output and the motion result go back to pinned host buffers, copies timed.
+roofline: the attention kernel, its flops per launch over its mean launch time (CUDA events on
+          the launch stream, inside the timed region), against the measured dense bf16 peak.
+cpu_baseline / --impl reference: the CPU oracle on the same workload, on a bounded sample of
+          query rows (its cost per row is fixed at a given key count).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth_inputs import WORKLOADS, stream_config_dict  # noqa: E402
+
+METRIC = "chunk-attention TFLOP/s & latent frames/s (Wan-1.3B 480p shape); % BF16 peak"
+PEAK_FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+VIDEO_FRAMES_PER_LATENT = 4          # Wan VAE: 4 video frames per latent frame in time
+VIDEO_SHAPE = (480, 832, 3)
+
+
+def describe(w):
+    return ("%s: %d streams, %d heads x %d, %dx%d = %d tokens/latent frame, chunk %d frames (%d queries), "
+            "sink %d + window %d frames (%d KV), %d layers x %d denoise steps per chunk"
+            % (w.name, w.batch, w.heads, w.head_dim, w.grid_h, w.grid_w, w.hw, w.chunk_frames, w.nq,
+               w.sink_frames, w.window_frames, w.slots * w.hw, w.layers, w.denoise_steps))
+
+
+# ------------------------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# ------------------------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self, gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl"
+            try:
+                import torch
+                if not torch.cuda.is_available():
+                    backend = "gloo"
+            except Exception:
+                backend = "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------
+# peaks, clocks, profile evidence
+# ------------------------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except Exception:
+        return dict(PEAK_FALLBACK), "fallback"
+
+
+def peak_value(d, key):
+    """Find a numeric peak in MEASURED_PEAKS.json whatever its nesting."""
+    if isinstance(d, dict):
+        if key in d and isinstance(d[key], (int, float)):
+            return float(d[key])
+        for v in d.values():
+            r = peak_value(v, key)
+            if r is not None:
+                return r
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def attention_source_hash():
+    h = hashlib.sha256()
+    for f in ("attention.cu", "ptx.cuh", "tmem_io.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "streaming_causal_video_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """dram bytes per attention launch from the committed ncu summary, if it matches this source."""
+    path = os.path.join(ROOT, "profiles", "chunk_attention_%s.json" % workload)
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except Exception:
+        return None
+    if d.get("source_hash") != attention_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle baseline
+# ------------------------------------------------------------------------------------------
+
+def oracle_sample(w, seconds_target, seed=0, max_rows=4096):
+    """Time the oracle's fp64 attention on query rows of the steady-state key count, growing the
+    sample until it has run about `seconds_target`.  Returns (flops, seconds, rows, threads)."""
+    import numpy as np
+    import oracle
+    from synth_inputs import qkv_chunk_bits
+    rng = np.random.default_rng(seed)
+    nkv = w.slots * w.hw
+    D = w.head_dim
+    # keys/values: N(0,1) bf16 bits for one head, the chunk's queries for the rows
+    q, k, _ = qkv_chunk_bits(w, 1, 0)
+    keys = np.ascontiguousarray(np.resize(k[0, :, 0, :], (nkv, D)))
+    vals = np.ascontiguousarray(np.resize(q[0, :, 1 % w.heads, :], (nkv, D)))
+    qrows = np.ascontiguousarray(q[0, :, 0, :])
+    rows_done, t_total, n = 0, 0.0, 8
+    while t_total < seconds_target and rows_done < max_rows:
+        rows = rng.choice(w.nq, size=n, replace=False)
+        t0 = time.perf_counter()
+        oracle.attention_bf16(qrows, keys, vals, 1.0 / math.sqrt(D), rows=rows)
+        t_total += time.perf_counter() - t0
+        rows_done += n
+        n = min(n * 2, 512)
+    flops = 4.0 * D * nkv * rows_done
+    return flops, t_total, rows_done, oracle.num_threads()
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+
+def run_ours(args, dist):
+    import torch
+    import streaming_causal_video_gb300 as sd
+    from synth_inputs import motion_frames_host
+
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    w = WORKLOADS[args.workload]
+    cfg = sd.StreamConfig.make(**stream_config_dict(w))
+    B, H, D, nq = w.batch, w.heads, w.head_dim, w.nq
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+
+    sess = sd.StreamSession(cfg, w.layers, w.start_frames, dev, stream)
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    qkv = [tuple(torch.randn((B, nq, H, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                 for _ in range(3)) for _ in range(w.layers)]
+    outs = [torch.empty((B, nq, H, D), dtype=torch.bfloat16, device=dev) for _ in range(w.layers)]
+    vf = VIDEO_FRAMES_PER_LATENT * w.chunk_frames
+    Hp, Wp, Cc = VIDEO_SHAPE
+    frames = motion_frames_host(B, vf + 1, Hp, Wp, Cc, seed=w.seed, device=dev)
+    ssd = torch.empty((B, vf), dtype=torch.int64, device=dev)
+    mrms = torch.empty((B, vf), dtype=torch.float32, device=dev)
+
+    steady = 0
+    while sd.visible_tokens(cfg, steady) < w.slots * w.hw:
+        steady += 1
+    # bring every layer's cache to the steady state (full sink + window)
+    for c in range(steady):
+        for l in range(w.layers):
+            q, k, v = qkv[l]
+            sess.layer_step(l, [c] * B, q, k, v, out=outs[l], stream=stream)
+    stream.synchronize()
+    sd.check_device_error(sess.ws, stream)
+
+    flops_per_call = [4.0 * H * D * nq * sd.visible_tokens(cfg, c) * B for c in range(steady + 1)]
+    chunk = [steady]
+
+    def step(ev_pairs=None):
+        c = chunk[0]
+        sd.motion_l2(frames, ssd, mrms, stream=stream)
+        for _s in range(w.denoise_steps):
+            for l in range(w.layers):
+                q, k, v = qkv[l]
+                sd.rope_append_kv(cfg, w.start_frames, [c] * B, q, k, v, sess.q_rot, sess.layers[l].k,
+                                  sess.layers[l].v, sess.layers[l].meta, sess.ws, stream)
+                if ev_pairs is not None:
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                sd.chunk_attention(cfg, [c] * B, sess.q_rot, sess.layers[l].k, sess.layers[l].v, outs[l],
+                                   sess.ws, stream=stream)
+                if ev_pairs is not None:
+                    e1.record(stream)
+                    ev_pairs.append((e0, e1))
+        chunk[0] += 1
+        return w.denoise_steps * w.layers * flops_per_call[-1]
+
+    launches_per_step = 3 + 2 * w.denoise_steps * w.layers
+    warmup = max(3, args.warmup)
+    for _ in range(warmup):
+        step()
+    stream.synchronize()
+    sd.check_device_error(sess.ws, stream)
+
+    # ---- device-resident timed region
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    ev_pairs = []
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += step(ev_pairs)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    sd.check_device_error(sess.ws, stream)
+    ms_max = dist.max(ms)
+    attn_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    attn_mean_ms = statistics.mean(attn_ms)
+    total_flops = flops * dist.world
+    value = total_flops / (ms_max * 1e-3) / 1e12
+    latent_fps = args.steps * w.chunk_frames * B * dist.world / (ms_max * 1e-3)
+
+    # ---- end-to-end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+        h_qkv = [tuple(pin(t) for t in qkv[l]) for l in range(w.layers)]
+        h_out = [torch.empty((B, nq, H, D), dtype=torch.bfloat16, pin_memory=True) for _ in range(w.layers)]
+        h_frames = pin(frames)
+        h_ssd = torch.empty((B, vf), dtype=torch.int64, pin_memory=True)
+        d_in = [tuple(torch.empty_like(t) for t in qkv[0]) for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in h_qkv[0]) * w.layers * w.denoise_steps + \
+            h_frames.numel()
+        d2h = h_out[0].numel() * 2 * w.layers * w.denoise_steps + h_ssd.numel() * 8
+
+        def e2e_step():
+            c = chunk[0]
+            frames.copy_(h_frames, non_blocking=True)
+            sd.motion_l2(frames, ssd, mrms, stream=stream)
+            h_ssd.copy_(ssd, non_blocking=True)
+            i = 0
+            for _s in range(w.denoise_steps):
+                for l in range(w.layers):
+                    q, k, v = d_in[i & 1]
+                    hq, hk, hv = h_qkv[l]
+                    q.copy_(hq, non_blocking=True)
+                    k.copy_(hk, non_blocking=True)
+                    v.copy_(hv, non_blocking=True)
+                    sess.layer_step(l, [c] * B, q, k, v, out=outs[l], stream=stream)
+                    h_out[l].copy_(outs[l], non_blocking=True)
+                    i += 1
+            chunk[0] += 1
+            return w.denoise_steps * w.layers * flops_per_call[-1]
+
+        for _ in range(warmup):
+            e2e_step()
+        stream.synchronize()
+        dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        f2 = 0.0
+        for _ in range(args.steps):
+            f2 += e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+        ms2 = dist.max(e0.elapsed_time(e1))
+        sd.check_device_error(sess.ws, stream)
+        e2e = {"value": round(f2 * dist.world / (ms2 * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(ms2 / args.steps, 3),
+               "latent_frames_per_s": round(args.steps * w.chunk_frames * B * dist.world / (ms2 * 1e-3), 3)}
+
+    peaks, peak_src = load_peaks()
+    peak = peak_value(peaks, "bf16_tflops_sustained") or PEAK_FALLBACK["bf16_tflops_sustained"]
+    attn_flops = flops_per_call[-1]
+    achieved = attn_flops / (attn_mean_ms * 1e-3) / 1e12
+    traffic = profiled_traffic(args.workload)
+    roofline = {"bound": "tensor", "kernel": "chunk_attention_kernel", "achieved": round(achieved, 2),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % peak_src,
+                "flops_per_launch": attn_flops, "mean_launch_ms": round(attn_mean_ms, 4),
+                "launches_timed": len(attn_ms)}
+
+    res = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": dist.world,
+           "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms_max / args.steps, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded N(0,1) bf16 q/k/v per layer; seeded moving-texture uint8 frames)",
+           "config": {"workload": describe(w), "global_batch": B * dist.world,
+                      "parallelism": "replicas" if dist.world > 1 else "single GPU",
+                      "l2": "inputs larger than L2: %d distinct layer caches (%.1f GB)"
+                            % (w.layers, 2 * sd.cache_bytes(cfg) * w.layers / 1e9),
+                      "step": "1 chunk: motion over %d video frames + %d denoise steps x %d layers x "
+                              "(rope_append_kv + chunk_attention) at steady state (Nkv=%d)"
+                              % (vf, w.denoise_steps, w.layers, w.slots * w.hw)},
+           "latent_frames_per_s": round(latent_fps, 3),
+           "pct_bf16_peak": round(100.0 * value / peak, 2),
+           "gpu_launches": launches_per_step * args.steps,
+           "clocks": clk, "roofline": roofline, "e2e": e2e, "impl": "ours"}
+    return res
+
+
+def cpu_baseline_entry(w, seconds=12.0):
+    flops, secs, rows, threads = oracle_sample(w, seconds)
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "fp64 oracle attention of %d query rows against the steady-state %d keys of one head "
+                      "(bf16 inputs), %.1f s; TFLOP/s counts the same 4*D*Nkv flops per row as the GPU metric"
+                      % (rows, w.slots * w.hw, secs)}
+
+
+def run_reference(args, dist):
+    """The oracle as the reference arm: each step is a bounded sample of the workload's attention."""
+    import oracle
+    w = WORKLOADS[args.workload]
+    warmup = max(3, args.warmup)
+    per_step = 2.0
+    for _ in range(warmup):
+        oracle_sample(w, per_step / 4, seed=1, max_rows=64)
+    flops = secs = 0.0
+    rows = 0
+    for s in range(args.steps):
+        f, t, r, threads = oracle_sample(w, per_step, seed=100 + s, max_rows=2048)
+        flops += f
+        secs += t
+        rows += r
+    value = flops / secs / 1e12
+    return {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": warmup, "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(w)}, "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": "per step: fp64 oracle attention of query rows against the steady-state "
+                                       "%d keys for about %.0f s; %d rows in all" % (w.slots * w.hw, per_step, rows)},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="wan13b_480p", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the workload's layer count (profiling runs only; 0 = workload's)")
+    args = ap.parse_args()
+    if args.layers:
+        import dataclasses
+        WORKLOADS[args.workload] = dataclasses.replace(WORKLOADS[args.workload], layers=args.layers)
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, None)), flush=True)
+        return 0
+
+    dist = Dist(args.gpus)
+    res = run_ours(args, dist)
+    if dist.rank == 0:
+        if dist.world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline_entry(WORKLOADS[args.workload])
+        print(json.dumps(res), flush=True)
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,198 @@
+/*
+ * sdv2.h -- C ABI of the GB300 (sm_103a) streaming causal-video chunk-attention library.
+ *
+ * One call sequence per DiT layer and denoise step of a streamed chunk:
+ *   sdv2_rope_append_kv   Causal-RoPE on the chunk's q and k, then k_rot and v written into the
+ *                         layer's fixed-size KV cache (pinned sink + rolling window of frames).
+ *   sdv2_chunk_attention  the chunk's queries attend to every valid cache row: sink + window,
+ *                         the chunk itself included.
+ * and, once per batch of input frames,
+ *   sdv2_motion_l2        squared L2 distance of adjacent video frames (motion magnitude).
+ *
+ * Conventions shared by every entry point:
+ *  - All device memory is allocated and owned by the caller.  The library never allocates
+ *    device memory and keeps no per-call state on the host.  Host arrays passed in are read
+ *    before the call returns.
+ *  - Work is enqueued asynchronously on the caller's CUDA stream (`stream`, a cudaStream_t
+ *    passed as void*; NULL = the legacy default stream).  No entry point synchronizes, except
+ *    sdv2_workspace_init and sdv2_check_device_error, which say so.
+ *  - Arguments are validated on the host before anything is launched; a rejected call
+ *    launches nothing and returns SDV2_ERR_INVALID_ARG or SDV2_ERR_UNSUPPORTED.  A failed
+ *    launch returns SDV2_ERR_CUDA.  sdv2_last_error() gives a one-line reason (per thread).
+ *  - Device pointers must be 16-byte aligned.
+ *  - bf16 means IEEE binary32 truncated to its upper 16 bits (bfloat16), stored as uint16.
+ *
+ * Notation (stream configuration): B streams, H heads, D = head_dim = 128, HW = grid_h*grid_w
+ * tokens per latent frame, F frames per chunk, Nq = F*HW queries per chunk, F_s sink frames,
+ * W window frames (the window includes the current chunk), R refresh period in chunks.
+ */
+#ifndef SDV2_H
+#define SDV2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SDV2_OK = 0,
+    SDV2_ERR_INVALID_ARG = 1,   /* a pointer, size or configuration field is invalid */
+    SDV2_ERR_UNSUPPORTED = 2,   /* valid but not built for (e.g. head_dim != 128, not sm_103) */
+    SDV2_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+    SDV2_ERR_TIMEOUT = 4        /* a bounded device-side wait gave up (see check_device_error) */
+} sdv2_status;
+
+/*
+ * Stream configuration, shared by all streams of a batch and by all layers.
+ *
+ * 3D RoPE ("Accelerating Video Generation Inference with Sequential-Parallel 3D Positional
+ * Encoding Using a Global Time Index", technical summary 2(나) and 2(다)): the head dims are
+ * split into consecutive segments of rope_t, rope_h and rope_w dims (t first); inside a
+ * segment of d dims, pair (2j, 2j+1) turns by pos * rope_base^(-2j/d), where pos is the time
+ * index t, the grid row h or the grid column w of the token.  rope_t + rope_h + rope_w must
+ * equal head_dim and each must be even.
+ *
+ * Time index (Causal-RoPE with a global time index; RoPE refresh of "StreamDiffusionV2",
+ * review page section 三): token n of chunk c of stream b lies in frame i = n / HW of the
+ * chunk; its time index is t = start_frame[b] + F*(c mod R) + i, or start_frame[b] + F*c + i
+ * when refresh_chunks R = 0.  Its grid position is h = (n mod HW) / grid_w, w = n mod grid_w.
+ *
+ * Cache (sink token + rolling KV cache, same review page section 三): frames are numbered per
+ * stream, f = c*F + i.  Frame f lives in slot f if f < F_s, else in slot F_s + (f - F_s) mod W.
+ * After chunk c has been appended the valid slots are exactly the prefix
+ * [0, n_vis) with n = (c+1)*F and n_vis = min(F_s, n) + min(W, max(0, n - F_s)).
+ */
+typedef struct {
+    int32_t batch;             /* B >= 1 streams                                               */
+    int32_t heads;             /* H >= 1                                                       */
+    int32_t head_dim;          /* D; only 128 is built                                         */
+    int32_t rope_t, rope_h, rope_w;
+    double rope_base;          /* > 1, e.g. 10000                                              */
+    int32_t grid_h, grid_w;    /* latent tokens per frame = grid_h * grid_w                    */
+    int32_t chunk_frames;      /* F >= 1                                                       */
+    int32_t sink_frames;       /* F_s >= 0                                                     */
+    int32_t window_frames;     /* W >= F                                                       */
+    int32_t refresh_chunks;    /* R >= 0 (0 = the offset never resets)                         */
+    int64_t qkv_token_stride;  /* elements between consecutive tokens of q, k, v; 0 = H*D      */
+} sdv2_stream_cfg;
+
+/* One cache slot's metadata: which frame it holds and with which RoPE time index its keys
+ * were rotated.  frame_id = -1 marks an empty slot. */
+typedef struct {
+    int64_t frame_id;
+    int64_t tpos;
+} sdv2_slot_meta;
+
+/* ---- sizes ------------------------------------------------------------------------------ */
+
+/* Bytes of the workspace: RoPE tables for the h and w axes plus a device error word.  The
+ * workspace belongs to one configuration; it may be shared by all layers and both calls. */
+size_t sdv2_workspace_bytes(const sdv2_stream_cfg* cfg);
+
+/* Bytes of ONE of the two cache tensors (k or v) of one layer:
+ * [B][H][(F_s+W)*HW][D] bf16 = B*H*(F_s+W)*HW*D*2. */
+size_t sdv2_cache_bytes(const sdv2_stream_cfg* cfg);
+
+/* Bytes of one layer's slot metadata: [B][F_s+W] sdv2_slot_meta. */
+size_t sdv2_meta_bytes(const sdv2_stream_cfg* cfg);
+
+/* Valid KV rows n_vis*HW that chunk `chunk_index` attends to (formula in the struct comment);
+ * -1 on an invalid configuration or a negative chunk index. */
+int64_t sdv2_visible_tokens(const sdv2_stream_cfg* cfg, int64_t chunk_index);
+
+/* ---- set-up ----------------------------------------------------------------------------- */
+
+/* Fill the workspace: fp32 cos/sin tables of the h and w axes (angles and cos/sin in fp64 on
+ * the host, rounded once to fp32) and a cleared error word.  Enqueues copies on `stream` and
+ * synchronizes it before returning.  ws: device, sdv2_workspace_bytes(cfg) bytes. */
+sdv2_status sdv2_workspace_init(const sdv2_stream_cfg* cfg, void* ws, void* stream);
+
+/* Make one layer's cache empty: every slot's frame_id = -1, tpos = 0, and k and v zero.
+ * k_cache, v_cache: device, sdv2_cache_bytes(cfg) each; meta: device, sdv2_meta_bytes(cfg). */
+sdv2_status sdv2_cache_reset(const sdv2_stream_cfg* cfg, void* k_cache, void* v_cache, void* meta,
+                             void* stream);
+
+/* ---- the hot path ----------------------------------------------------------------------- */
+
+/*
+ * Causal-RoPE + cache append for chunk chunk_index[b] of every stream b.
+ *
+ * start_frame, chunk_index: HOST arrays of B int64 (>= 0): the global start frame S_b of
+ *   stream b and the chunk being appended.  Positions are derived as in the struct comment.
+ * q, k, v: device bf16, token-major [B][Nq][H][D], with qkv_token_stride elements between
+ *   consecutive tokens (so a packed [token][3][H][D] projection output can be passed as three
+ *   pointers) and Nq*stride elements between streams.
+ * q_rot: device bf16, [B][H][Nq][D] (head-major, the layout sdv2_chunk_attention reads).
+ * k_cache, v_cache: device bf16 [B][H][(F_s+W)*HW][D].  The F frames of the chunk are written
+ *   to their slots: k rotated, v copied.  Rows of other slots are not touched.
+ * meta: device [B][F_s+W] sdv2_slot_meta; the chunk's slots get frame_id = c*F + i and tpos.
+ * ws: device workspace from sdv2_workspace_init for the same configuration.
+ *
+ * Rounding (bit-exact contract): for each pair (x, y) with table values c, s (fp32),
+ *   x' = bf16_rne(fmaf(x, c, -(y*s))),  y' = bf16_rne(fmaf(x, s, y*c)),
+ * where y*s and y*c are single fp32 products.
+ * Calling it again for the same chunk (the next denoise step) overwrites the same slots.
+ * Limits: B*F*rope_t/2 <= 1536 (the time-axis table travels in the launch parameters).
+ */
+sdv2_status sdv2_rope_append_kv(const sdv2_stream_cfg* cfg, const int64_t* start_frame,
+                                const int64_t* chunk_index, const void* q, const void* k,
+                                const void* v, void* q_rot, void* k_cache, void* v_cache,
+                                void* meta, void* ws, void* stream);
+
+/*
+ * Chunk attention: out[b][n][h][:] = sum_j softmax_j(scale * <q_rot[b][h][n], k_j>) v_j over
+ * the valid cache rows j < sdv2_visible_tokens(cfg, chunk_index[b]) of stream b, head h.
+ * There is no mask inside the valid rows: the chunk attends to itself in full and to every
+ * retained earlier frame (chunk-causal attention of a Self-Forcing-style streaming DiT).
+ *
+ * chunk_index: HOST array of B int64 (>= 0).
+ * q_rot: device bf16 [B][H][Nq][D]; k_cache, v_cache: device bf16 [B][H][(F_s+W)*HW][D].
+ * scale: softmax scale; <= 0 selects 1/sqrt(D).
+ * out: device bf16 [B][Nq][H][D] (token-major, ready for the output projection).
+ * lse: device fp32 [B][H][Nq] natural-log log-sum-exp of the scaled scores, or NULL.
+ * ws: device workspace (holds the error word of the bounded waits).
+ * Numerics: bf16 tensor-core products with fp32 accumulation, online softmax in fp32.
+ * Limits: B <= 16; the device must be sm_103 (tcgen05 tensor cores).
+ */
+sdv2_status sdv2_chunk_attention(const sdv2_stream_cfg* cfg, const int64_t* chunk_index,
+                                 const void* q_rot, const void* k_cache, const void* v_cache,
+                                 float scale, void* out, float* lse, void* ws, void* stream);
+
+/*
+ * Motion magnitude of adjacent frames ("StreamDiffusionV2" review page, section 二 table and
+ * section 三: L2 motion estimation between adjacent frames feeds the noise controller).
+ *
+ * frames: device uint8 [B][T+1][Hp][Wp][C], contiguous.
+ * ssd: device uint64 [B][T]: ssd[b][t] = sum over pixels and channels of
+ *   (frames[b][t+1] - frames[b][t])^2, exact.
+ * m: device fp32 [B][T] or NULL: sqrt(ssd / (Hp*Wp*C)), the RMS pixel difference.
+ * Requires T >= 1 and Hp*Wp*C a multiple of 16.
+ */
+sdv2_status sdv2_motion_l2(const uint8_t* frames, int32_t B, int64_t T, int32_t Hp, int32_t Wp,
+                           int32_t C, uint64_t* ssd, float* m, void* stream);
+
+/* ---- errors ----------------------------------------------------------------------------- */
+
+/* Synchronizes `stream`, reads and clears the workspace's device error word, and returns
+ * SDV2_ERR_TIMEOUT if a bounded device wait gave up since the last check (the outputs of the
+ * calls involved are then undefined), SDV2_ERR_CUDA on a CUDA error, else SDV2_OK. */
+sdv2_status sdv2_check_device_error(void* ws, void* stream);
+
+/* Upper bound of every bounded device-side wait, in nanoseconds (default 2e9).  Applies to
+ * launches made after the call, from any thread. */
+void sdv2_set_wait_timeout_ns(uint64_t ns);
+
+/* Fault injection for tests of the bounded waits: when tile >= 0, the next
+ * sdv2_chunk_attention launches skip the copy of KV tile `tile` (the consumers' waits then
+ * run out, the kernel records SDV2_ERR_TIMEOUT and returns).  -1 turns it off. */
+void sdv2_debug_drop_kv_tile(int64_t tile);
+
+const char* sdv2_status_string(sdv2_status s);
+const char* sdv2_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SDV2_H */

@@ -1,0 +1,188 @@
+"""ctypes binding of libsdv2.so (argument marshalling only)."""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "libsdv2.so")
+_LIB = None
+
+SDV2_OK = 0
+STATUS_NAMES = {0: "SDV2_OK", 1: "SDV2_ERR_INVALID_ARG", 2: "SDV2_ERR_UNSUPPORTED", 3: "SDV2_ERR_CUDA",
+                4: "SDV2_ERR_TIMEOUT"}
+
+# Every symbol that include/sdv2.h declares.
+EXPORTS = ["sdv2_workspace_bytes", "sdv2_cache_bytes", "sdv2_meta_bytes", "sdv2_visible_tokens",
+           "sdv2_workspace_init", "sdv2_cache_reset", "sdv2_rope_append_kv", "sdv2_chunk_attention",
+           "sdv2_motion_l2", "sdv2_check_device_error", "sdv2_set_wait_timeout_ns",
+           "sdv2_debug_drop_kv_tile", "sdv2_status_string", "sdv2_last_error"]
+
+
+class SDV2Error(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__("%s: %s (%s)" % (where, STATUS_NAMES.get(status, str(status)), detail))
+
+
+class StreamConfig(ctypes.Structure):
+    """Mirror of sdv2_stream_cfg."""
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("rope_t", ctypes.c_int32), ("rope_h", ctypes.c_int32), ("rope_w", ctypes.c_int32),
+                ("rope_base", ctypes.c_double), ("grid_h", ctypes.c_int32), ("grid_w", ctypes.c_int32),
+                ("chunk_frames", ctypes.c_int32), ("sink_frames", ctypes.c_int32),
+                ("window_frames", ctypes.c_int32), ("refresh_chunks", ctypes.c_int32),
+                ("qkv_token_stride", ctypes.c_int64)]
+
+    @classmethod
+    def make(cls, **kw):
+        c = cls()
+        for k, v in kw.items():
+            setattr(c, k, v)
+        return c
+
+    @property
+    def hw(self):
+        return self.grid_h * self.grid_w
+
+    @property
+    def nq(self):
+        return self.chunk_frames * self.hw
+
+    @property
+    def slots(self):
+        return self.sink_frames + self.window_frames
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded library.  Raises if libsdv2.so has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("libsdv2.so is not built; run __graft_entry__.build() or "
+                               "python -m streaming_causal_video_gb300.build")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i64, u64, i32, cfgp = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int32,
+                                   ctypes.POINTER(StreamConfig))
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        for name in ("sdv2_workspace_bytes", "sdv2_cache_bytes", "sdv2_meta_bytes"):
+            getattr(L, name).restype = ctypes.c_size_t
+            getattr(L, name).argtypes = [cfgp]
+        L.sdv2_visible_tokens.restype = i64
+        L.sdv2_visible_tokens.argtypes = [cfgp, i64]
+        L.sdv2_workspace_init.restype = ctypes.c_int
+        L.sdv2_workspace_init.argtypes = [cfgp, vp, vp]
+        L.sdv2_cache_reset.restype = ctypes.c_int
+        L.sdv2_cache_reset.argtypes = [cfgp, vp, vp, vp, vp]
+        L.sdv2_rope_append_kv.restype = ctypes.c_int
+        L.sdv2_rope_append_kv.argtypes = [cfgp, i64p, i64p, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.sdv2_chunk_attention.restype = ctypes.c_int
+        L.sdv2_chunk_attention.argtypes = [cfgp, i64p, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
+        L.sdv2_motion_l2.restype = ctypes.c_int
+        L.sdv2_motion_l2.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp, vp]
+        L.sdv2_check_device_error.restype = ctypes.c_int
+        L.sdv2_check_device_error.argtypes = [vp, vp]
+        L.sdv2_set_wait_timeout_ns.restype = None
+        L.sdv2_set_wait_timeout_ns.argtypes = [u64]
+        L.sdv2_debug_drop_kv_tile.restype = None
+        L.sdv2_debug_drop_kv_tile.argtypes = [i64]
+        L.sdv2_status_string.restype = ctypes.c_char_p
+        L.sdv2_status_string.argtypes = [ctypes.c_int]
+        L.sdv2_last_error.restype = ctypes.c_char_p
+        L.sdv2_last_error.argtypes = []
+        _LIB = L
+    return _LIB
+
+
+def exported_symbols():
+    """Names from include/sdv2.h that the loaded library resolves."""
+    L = lib()
+    return [n for n in EXPORTS if hasattr(L, n)]
+
+
+def _check(status: int, where: str):
+    if status != SDV2_OK:
+        raise SDV2Error(status, where, lib().sdv2_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _i64_array(values, n):
+    vals = [int(x) for x in values]
+    if len(vals) != n:
+        raise ValueError("expected %d values, got %d" % (n, len(vals)))
+    return (ctypes.c_int64 * n)(*vals)
+
+
+def workspace_bytes(cfg: StreamConfig) -> int:
+    return lib().sdv2_workspace_bytes(ctypes.byref(cfg))
+
+
+def cache_bytes(cfg: StreamConfig) -> int:
+    return lib().sdv2_cache_bytes(ctypes.byref(cfg))
+
+
+def meta_bytes(cfg: StreamConfig) -> int:
+    return lib().sdv2_meta_bytes(ctypes.byref(cfg))
+
+
+def visible_tokens(cfg: StreamConfig, chunk_index: int) -> int:
+    return lib().sdv2_visible_tokens(ctypes.byref(cfg), int(chunk_index))
+
+
+def workspace_init(cfg, ws, stream=None):
+    _check(lib().sdv2_workspace_init(ctypes.byref(cfg), _ptr(ws), _stream(stream)), "sdv2_workspace_init")
+
+
+def cache_reset(cfg, k_cache, v_cache, meta, stream=None):
+    _check(lib().sdv2_cache_reset(ctypes.byref(cfg), _ptr(k_cache), _ptr(v_cache), _ptr(meta), _stream(stream)),
+           "sdv2_cache_reset")
+
+
+def rope_append_kv(cfg, start_frame, chunk_index, q, k, v, q_rot, k_cache, v_cache, meta, ws, stream=None):
+    B = cfg.batch
+    _check(lib().sdv2_rope_append_kv(ctypes.byref(cfg), _i64_array(start_frame, B), _i64_array(chunk_index, B),
+                                     _ptr(q), _ptr(k), _ptr(v), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(meta), _ptr(ws), _stream(stream)), "sdv2_rope_append_kv")
+
+
+def chunk_attention(cfg, chunk_index, q_rot, k_cache, v_cache, out, ws, lse=None, scale=0.0, stream=None):
+    _check(lib().sdv2_chunk_attention(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch), _ptr(q_rot),
+                                      _ptr(k_cache), _ptr(v_cache), float(scale), _ptr(out), _ptr(lse), _ptr(ws),
+                                      _stream(stream)), "sdv2_chunk_attention")
+
+
+def motion_l2(frames, ssd, m=None, stream=None):
+    """frames: uint8 [B][T+1][Hp][Wp][C] on the device; ssd: uint64-sized [B][T]; m: fp32 [B][T]."""
+    B, T1, Hp, Wp, C = frames.shape
+    _check(lib().sdv2_motion_l2(_ptr(frames), B, T1 - 1, Hp, Wp, C, _ptr(ssd), _ptr(m), _stream(stream)),
+           "sdv2_motion_l2")
+
+
+def check_device_error(ws, stream=None):
+    _check(lib().sdv2_check_device_error(_ptr(ws), _stream(stream)), "sdv2_check_device_error")
+
+
+def set_wait_timeout_ns(ns: int):
+    lib().sdv2_set_wait_timeout_ns(int(ns))
+
+
+def debug_drop_kv_tile(tile: int):
+    lib().sdv2_debug_drop_kv_tile(int(tile))

@@ -1,0 +1,430 @@
+// Chunk attention on the 5th-generation tensor cores (tcgen05 + tensor memory) of sm_103a.
+//
+// What it computes: the chunk's queries attend, with no mask, to every valid row of the layer's
+// KV cache -- the sink frames, the rolling window and the chunk itself -- which is the
+// chunk-causal attention of a Self-Forcing-style autoregressive video DiT ("Accelerating Video
+// Generation Inference with Sequential-Parallel 3D Positional Encoding Using a Global Time
+// Index", technical summary sections 1 and 2(가): causal autoregressive generation with KV
+// caching; "StreamDiffusionV2" review page, section 三: sink tokens + rolling KV cache).
+//   out[b, n, h, :] = sum_j softmax_j(scale * q_rot[b, h, n, :] . k[b, h, j, :]) v[b, h, j, :]
+//
+// How (one CTA = one head of one stream and two 128-row query tiles):
+//   warp 8 (TMA)      : Q tiles once, then K and V tiles of 128 keys through 2-stage rings.
+//                       3D tensor maps per stream clip the key range at the valid prefix, so
+//                       rows past it arrive as zeros; 128-byte swizzled boxes of 64 dims.
+//   warp 9 (MMA)      : one thread issues tcgen05.mma.  S_t = Q_t K^T (A and B from shared
+//                       memory, K-major) into tensor memory; O_t += P_t V (A = P from tensor
+//                       memory, B = V from shared memory, MN-major).  Completion is signalled
+//                       with tcgen05.commit on mbarriers.
+//   warps 0-3, 4-7    : one softmax warpgroup per query tile; thread = query row = TMEM lane.
+//                       Online softmax in fp32 with a lazily updated running max (the output
+//                       accumulator in tensor memory is rescaled only when the max grows by more
+//                       than 2^8), P written back into the S columns as packed bf16.
+// Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1, 128 fp32 columns each.
+// The two tiles ping-pong: while one warpgroup turns S_t into P_t, the tensor core runs the
+// other tile's PV and next QK^T.  Because tcgen05 operations issued by one thread complete in
+// order and a commit covers all earlier ones, the arrival of S_t(j) also proves that
+// O_t += P_t(j-1) V(j-1) has finished, so O_t can be rescaled without another barrier.
+//
+// Every mbarrier wait is bounded (globaltimer); on expiry the kernel records kErrTimeout in
+// the workspace error word, tells the other roles to stop, drains its own copies and MMAs and
+// frees its tensor memory before returning.
+#include <cuda_bf16.h>
+
+#include <atomic>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sdv2 {
+namespace {
+
+constexpr int BM = 128;                 // query rows per tile
+constexpr int BN = 128;                 // keys per KV tile
+constexpr int HD = 128;                 // head dim
+constexpr int NQT = 2;                  // query tiles per CTA
+constexpr int KST = 2;                  // K stages
+constexpr int VST = 2;                  // V stages
+constexpr uint32_t TILE = BM * HD * 2;  // 32 KB
+constexpr uint32_t HALF = TILE / 2;     // one 64-dim box: 128 rows x 128 bytes
+constexpr int TMA_WARP = 4 * NQT;
+constexpr int MMA_WARP = 4 * NQT + 1;
+constexpr int NTHREADS = (4 * NQT + 2) * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+// barrier indices
+constexpr int B_QFULL = 0;
+constexpr int B_KFULL = 1;
+constexpr int B_KEMPTY = B_KFULL + KST;
+constexpr int B_VFULL = B_KEMPTY + KST;
+constexpr int B_VEMPTY = B_VFULL + VST;
+constexpr int B_SFULL = B_VEMPTY + VST;
+constexpr int B_PFULL = B_SFULL + NQT;
+constexpr int B_OFULL = B_PFULL + NQT;
+constexpr int B_MMADONE = B_OFULL + NQT;
+constexpr int NBARS = B_MMADONE + 1;
+
+constexpr uint32_t SMEM_TILES = (NQT + KST + VST) * TILE;
+constexpr uint32_t SMEM_BYTES = SMEM_TILES + 1024 /* barriers, flags */ + 1024 /* alignment */;
+
+__device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(t * 128); }
+__device__ __forceinline__ uint32_t o_col(int t) { return static_cast<uint32_t>((NQT + t) * 128); }
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag, uint32_t* err)
+{
+    *abort_flag = 1;
+    atomicOr(err, kErrTimeout);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __grid_constant__ AttnParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sK = sQ + NQT * TILE;
+    const uint32_t sV = sK + KST * TILE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_TILES);
+    const uint32_t bar0 = smem_u32(bars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+#define BAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
+
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
+    const int lane = threadIdx.x & 31;
+    const int h = blockIdx.y;
+    const int b = blockIdx.z;
+    const int nkv = p.nkv[b];
+    const int ntiles = (nkv + BN - 1) / BN;
+    const int q0 = blockIdx.x * (BM * NQT);
+    const uint64_t tmo = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(B_QFULL), 1);
+        for (int i = 0; i < KST; ++i) { mbar_init(BAR(B_KFULL + i), 1); mbar_init(BAR(B_KEMPTY + i), 1); }
+        for (int i = 0; i < VST; ++i) { mbar_init(BAR(B_VFULL + i), 1); mbar_init(BAR(B_VEMPTY + i), 1); }
+        for (int t = 0; t < NQT; ++t) {
+            mbar_init(BAR(B_SFULL + t), 1);
+            mbar_init(BAR(B_PFULL + t), 128);
+            mbar_init(BAR(B_OFULL + t), 1);
+        }
+        mbar_init(BAR(B_MMADONE), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == TMA_WARP) {
+        // ------------------------------------------------------------------ producer (TMA)
+        if (lane == 0) {
+            const CUtensorMap* qm = &p.qmap;
+            const CUtensorMap* km = &p.kmap[b];
+            const CUtensorMap* vm = &p.vmap[b];
+            tma_prefetch_desc(qm);
+            tma_prefetch_desc(km);
+            tma_prefetch_desc(vm);
+            const int plane = b * p.H + h;
+            mbar_arrive_expect_tx(BAR(B_QFULL), NQT * TILE);
+            for (int t = 0; t < NQT; ++t)
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_load_3d(sQ + t * TILE + hf * HALF, qm, BAR(B_QFULL), hf * 64, q0 + t * BM, plane);
+            int kpend[KST] = {}, vpend[VST] = {};
+            uint32_t kpar[KST] = {}, vpar[VST] = {};
+            for (int j = 0; j < ntiles; ++j) {
+                const int ks = j % KST;
+                const uint32_t kph = static_cast<uint32_t>(j / KST) & 1u;
+                if (!mbar_wait_bounded(BAR(B_KEMPTY + ks), kph ^ 1u, tmo, abort_flag)) { raise_abort(abort_flag, p.err); break; }
+                if (j != p.drop_tile) {
+                    mbar_arrive_expect_tx(BAR(B_KFULL + ks), TILE);
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d(sK + ks * TILE + hf * HALF, km, BAR(B_KFULL + ks), hf * 64, j * BN, h);
+                    kpend[ks] = 1;
+                    kpar[ks] = kph;
+                }
+                const int vs = j % VST;
+                const uint32_t vph = static_cast<uint32_t>(j / VST) & 1u;
+                if (!mbar_wait_bounded(BAR(B_VEMPTY + vs), vph ^ 1u, tmo, abort_flag)) { raise_abort(abort_flag, p.err); break; }
+                if (j != p.drop_tile) {
+                    mbar_arrive_expect_tx(BAR(B_VFULL + vs), TILE);
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d(sV + vs * TILE + hf * HALF, vm, BAR(B_VFULL + vs), hf * 64, j * BN, h);
+                    vpend[vs] = 1;
+                    vpar[vs] = vph;
+                }
+            }
+            // Drain: every copy this thread started must land before the CTA may exit.
+            volatile int no_abort = 0;
+            mbar_wait_bounded(BAR(B_QFULL), 0, tmo, &no_abort);
+            for (int i = 0; i < KST; ++i)
+                if (kpend[i]) mbar_wait_bounded(BAR(B_KFULL + i), kpar[i], tmo, &no_abort);
+            for (int i = 0; i < VST; ++i)
+                if (vpend[i]) mbar_wait_bounded(BAR(B_VFULL + i), vpar[i], tmo, &no_abort);
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t idO = idesc_bf16_f32(BM, HD, true);
+            auto issue_s = [&](int t, int ks) {
+#pragma unroll
+                for (int k = 0; k < HD / 16; ++k) {
+                    const uint32_t off = static_cast<uint32_t>(k >> 2) * HALF + static_cast<uint32_t>(k & 3) * 32u;
+                    const uint64_t a = sdesc_sw128(sQ + t * TILE + off, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(sK + ks * TILE + off, 16, 1024);
+                    mma_ss(tmem + s_col(t), a, bd, idS, k > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int vs, bool acc) {
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    const uint64_t bd = sdesc_sw128(sV + vs * TILE + static_cast<uint32_t>(k) * 2048u, HALF, 1024);
+                    mma_ts(tmem + o_col(t), tmem + s_col(t) + static_cast<uint32_t>(k) * 8u, bd, idO,
+                           (acc || k > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = mbar_wait_bounded(BAR(B_QFULL), 0, tmo, abort_flag) &&
+                      mbar_wait_bounded(BAR(B_KFULL + 0), 0, tmo, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < NQT; ++t) {
+                    issue_s(t, 0);
+                    mma_commit(BAR(B_SFULL + t));
+                }
+                mma_commit(BAR(B_KEMPTY + 0));
+            }
+            for (int j = 0; ok && j < ntiles; ++j) {
+                const int vs = j % VST;
+                if (!mbar_wait_bounded(BAR(B_VFULL + vs), static_cast<uint32_t>(j / VST) & 1u, tmo, abort_flag)) { ok = false; break; }
+                const bool more = j + 1 < ntiles;
+                const int ks = (j + 1) % KST;
+                for (int t = 0; t < NQT; ++t) {
+                    if (!mbar_wait_bounded(BAR(B_PFULL + t), static_cast<uint32_t>(j) & 1u, tmo, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(t, vs, j > 0);
+                    if (!more) mma_commit(BAR(B_OFULL + t));
+                    if (more) {
+                        if (t == 0 &&
+                            !mbar_wait_bounded(BAR(B_KFULL + ks), static_cast<uint32_t>((j + 1) / KST) & 1u, tmo, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_s(t, ks);
+                        mma_commit(BAR(B_SFULL + t));
+                    }
+                }
+                if (!ok) break;
+                mma_commit(BAR(B_VEMPTY + vs));
+                if (more) mma_commit(BAR(B_KEMPTY + ks));
+            }
+            if (!ok) raise_abort(abort_flag, p.err);
+            // Drain: all MMAs issued by this thread complete before tensor memory is freed.
+            mma_commit(BAR(B_MMADONE));
+            volatile int no_abort = 0;
+            mbar_wait_bounded(BAR(B_MMADONE), 0, tmo, &no_abort);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ softmax warpgroups
+        const int t = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_base + s_col(t);
+        const uint32_t tO = tmem + lane_base + o_col(t);
+        const float sl2 = p.scale_log2;
+        float m_run = -INFINITY;
+        float l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            if (!mbar_wait_bounded(BAR(B_SFULL + t), static_cast<uint32_t>(j) & 1u, tmo, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t r[128];
+            tmem_ld_x128_sync(tS, r);
+            const int valid = min(BN, nkv - j * BN);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 128; ++i) {
+                float x = __uint_as_float(r[i]) * sl2;
+                if (i >= valid) x = -INFINITY;
+                r[i] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
+            }
+            const float m_new = fmaxf(m_run, mx);
+            const bool grow = m_new > m_run + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float f = grow ? ex2_approx(m_run - m_new) : 1.0f;
+                if (j > 0) {
+                    // O_t is stable here: S_t(j) was committed after O_t += P_t(j-1) V(j-1).
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld_x32_sync(tO + c * 32, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                        tmem_st_x32(tO + c * 32, o);
+                    }
+                }
+                if (grow) {
+                    l_run *= f;
+                    m_run = m_new;
+                }
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ex2_approx(__uint_as_float(r[hf * 64 + 2 * i]) - m_run);
+                    const float p1 = ex2_approx(__uint_as_float(r[hf * 64 + 2 * i + 1]) - m_run);
+                    sum += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st_x32(tS + hf * 32, pk);
+            }
+            l_run += sum;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(B_PFULL + t));
+        }
+        if (!ok) {
+            raise_abort(abort_flag, p.err);
+        } else if (mbar_wait_bounded(BAR(B_OFULL + t), 0, tmo, abort_flag)) {
+            tc_fence_after();
+            const int q = q0 + t * BM + row;
+            const float inv = 1.0f / l_run;
+            uint16_t* dst = p.out + ((static_cast<int64_t>(b) * p.Nq + q) * p.H + h) * HD;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                tmem_ld_x32_sync(tO + c * 32, o);
+                if (q < p.Nq) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                        d4[v] = w;
+                    }
+                }
+            }
+            if (p.lse && q < p.Nq)
+                p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + q] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+        } else {
+            raise_abort(abort_flag, p.err);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+#undef BAR
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// (D = 128 dims, rows, planes) bf16 tensor with row stride 256 bytes; boxes of 64 dims x 128 rows.
+bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t planes, int64_t plane_stride_bytes)
+{
+    EncodeTiledFn enc = get_encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(planes)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(HD * 2), static_cast<cuuint64_t>(plane_stride_bytes)};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BM), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cache, const uint16_t* v_cache, int B,
+                                   int H, int Nq, int64_t rows_per_head, const int32_t* nkv, float scale,
+                                   uint16_t* out, float* lse, uint32_t* err, uint64_t timeout_ns, int64_t drop_tile,
+                                   cudaStream_t s, const char** why)
+{
+    AttnParams p{};   // about 4.3 KB; passed by value as the launch's parameter block
+    if (!encode_rows_map(&p.qmap, q_rot, Nq, static_cast<int64_t>(B) * H, static_cast<int64_t>(Nq) * HD * 2)) {
+        *why = "cuTensorMapEncodeTiled failed for q_rot";
+        return cudaErrorInvalidValue;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int64_t off = static_cast<int64_t>(b) * H * rows_per_head * HD;
+        if (!encode_rows_map(&p.kmap[b], k_cache + off, nkv[b], H, rows_per_head * HD * 2) ||
+            !encode_rows_map(&p.vmap[b], v_cache + off, nkv[b], H, rows_per_head * HD * 2)) {
+            *why = "cuTensorMapEncodeTiled failed for the KV cache";
+            return cudaErrorInvalidValue;
+        }
+        p.nkv[b] = nkv[b];
+    }
+    p.out = out;
+    p.lse = lse;
+    p.err = err;
+    p.B = B;
+    p.H = H;
+    p.Nq = Nq;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.timeout_ns = timeout_ns;
+    p.drop_tile = drop_tile;
+
+    static std::atomic<uint64_t> attr_set{0};   // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = uint64_t(1) << (dev & 63);
+    if (!(attr_set.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(SMEM_BYTES));
+        if (e != cudaSuccess) {
+            *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+            return e;
+        }
+        attr_set.fetch_or(bit);
+    }
+    dim3 grid(static_cast<unsigned>((Nq + BM * NQT - 1) / (BM * NQT)), static_cast<unsigned>(H),
+              static_cast<unsigned>(B));
+    chunk_attention_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace sdv2

@@ -1,0 +1,332 @@
+// C ABI of the library: argument validation, host-side RoPE tables, and dispatch to the kernels.
+//
+// RoPE frequencies follow the 3D rotary embedding of a Wan-style DiT with the time index of
+// Causal-RoPE ("Accelerating Video Generation Inference with Sequential-Parallel 3D Positional
+// Encoding Using a Global Time Index", technical summary 2(나), 2(다)): the angle of pair j of an
+// axis of d dims at position pos is pos * base^(-2j/d), evaluated in fp64, and the table holds
+// the fp64 cos/sin rounded once to fp32 (precomputed contiguous tables instead of a cache).
+// The RoPE refresh ("StreamDiffusionV2" review page, section 三) resets the chunk offset of the
+// time index every R chunks.
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int64_t> g_drop_tile{-1};
+
+constexpr size_t kErrBytes = 256;   // error word region at the start of the workspace
+
+sdv2_status fail(sdv2_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+sdv2_status fail(sdv2_status s, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+sdv2_status ok()
+{
+    g_last_error[0] = 0;
+    return SDV2_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+sdv2_status check_cfg(const sdv2_stream_cfg* c)
+{
+    if (!c) return fail(SDV2_ERR_INVALID_ARG, "cfg is NULL");
+    if (c->batch < 1 || c->heads < 1) return fail(SDV2_ERR_INVALID_ARG, "batch and heads must be >= 1");
+    if (c->rope_t < 0 || c->rope_h < 0 || c->rope_w < 0 || (c->rope_t | c->rope_h | c->rope_w) & 1)
+        return fail(SDV2_ERR_INVALID_ARG, "rope_t, rope_h, rope_w must be even and >= 0");
+    if (c->rope_t + c->rope_h + c->rope_w != c->head_dim)
+        return fail(SDV2_ERR_INVALID_ARG, "rope_t + rope_h + rope_w (%d) != head_dim (%d)",
+                    c->rope_t + c->rope_h + c->rope_w, c->head_dim);
+    if (c->head_dim != 128) return fail(SDV2_ERR_UNSUPPORTED, "only head_dim 128 is built (got %d)", c->head_dim);
+    if (!(c->rope_base > 1.0) || !std::isfinite(c->rope_base)) return fail(SDV2_ERR_INVALID_ARG, "rope_base must be > 1");
+    if (c->grid_h < 1 || c->grid_w < 1) return fail(SDV2_ERR_INVALID_ARG, "grid_h and grid_w must be >= 1");
+    if (c->chunk_frames < 1) return fail(SDV2_ERR_INVALID_ARG, "chunk_frames must be >= 1");
+    if (c->sink_frames < 0) return fail(SDV2_ERR_INVALID_ARG, "sink_frames must be >= 0");
+    if (c->window_frames < c->chunk_frames)
+        return fail(SDV2_ERR_INVALID_ARG, "window_frames (%d) must be >= chunk_frames (%d)", c->window_frames,
+                    c->chunk_frames);
+    if (c->refresh_chunks < 0) return fail(SDV2_ERR_INVALID_ARG, "refresh_chunks must be >= 0");
+    const int64_t hw = static_cast<int64_t>(c->grid_h) * c->grid_w;
+    const int64_t rows = (static_cast<int64_t>(c->sink_frames) + c->window_frames) * hw;
+    const int64_t nq = hw * c->chunk_frames;
+    if (rows > (int64_t(1) << 30) || nq > (int64_t(1) << 30))
+        return fail(SDV2_ERR_INVALID_ARG, "cache rows per head (%lld) or chunk tokens (%lld) exceed 2^30",
+                    (long long)rows, (long long)nq);
+    const int64_t stride = c->qkv_token_stride ? c->qkv_token_stride : int64_t(c->heads) * c->head_dim;
+    if (stride < int64_t(c->heads) * c->head_dim || (stride & 7))
+        return fail(SDV2_ERR_INVALID_ARG, "qkv_token_stride (%lld) must be >= H*D and a multiple of 8",
+                    (long long)stride);
+    return SDV2_OK;
+}
+
+int64_t hw_of(const sdv2_stream_cfg* c) { return static_cast<int64_t>(c->grid_h) * c->grid_w; }
+int64_t slots_of(const sdv2_stream_cfg* c) { return static_cast<int64_t>(c->sink_frames) + c->window_frames; }
+
+int64_t visible_frames(const sdv2_stream_cfg* c, int64_t chunk)
+{
+    const int64_t n = (chunk + 1) * c->chunk_frames;
+    const int64_t fs = c->sink_frames, w = c->window_frames;
+    return std::min(fs, n) + std::min(w, std::max<int64_t>(0, n - fs));
+}
+
+int64_t slot_of(const sdv2_stream_cfg* c, int64_t frame)
+{
+    if (frame < c->sink_frames) return frame;
+    return c->sink_frames + (frame - c->sink_frames) % c->window_frames;
+}
+
+double omega(int j, int d, double base) { return std::pow(base, -static_cast<double>(2 * j) / static_cast<double>(d)); }
+
+void cos_sin_f32(int64_t pos, int j, int d, double base, float* cs)
+{
+    const double th = static_cast<double>(pos) * omega(j, d, base);
+    cs[0] = static_cast<float>(std::cos(th));
+    cs[1] = static_cast<float>(std::sin(th));
+}
+
+// sm_103 check, cached per device.
+sdv2_status check_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(SDV2_ERR_CUDA, "cudaGetDevice failed");
+    static int8_t known[64] = {};
+    if (dev < 0 || dev >= 64) return fail(SDV2_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    if (known[dev] == 0) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        known[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (known[dev] < 0) return fail(SDV2_ERR_UNSUPPORTED, "the library is built for sm_103a (GB300) only");
+    return SDV2_OK;
+}
+
+sdv2_status cuda_status(cudaError_t e, const char* what)
+{
+    if (e == cudaSuccess) return ok();
+    return fail(SDV2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sdv2_status_string(sdv2_status s)
+{
+    switch (s) {
+    case SDV2_OK: return "ok";
+    case SDV2_ERR_INVALID_ARG: return "invalid argument";
+    case SDV2_ERR_UNSUPPORTED: return "unsupported";
+    case SDV2_ERR_CUDA: return "CUDA error";
+    case SDV2_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+const char* sdv2_last_error(void) { return g_last_error; }
+
+void sdv2_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+void sdv2_debug_drop_kv_tile(int64_t tile) { g_drop_tile.store(tile < 0 ? -1 : tile); }
+
+size_t sdv2_workspace_bytes(const sdv2_stream_cfg* c)
+{
+    if (check_cfg(c) != SDV2_OK) return 0;
+    return kErrBytes + round_up(sizeof(float2) * c->grid_h * (c->rope_h / 2), 256) +
+           round_up(sizeof(float2) * c->grid_w * (c->rope_w / 2), 256);
+}
+
+size_t sdv2_cache_bytes(const sdv2_stream_cfg* c)
+{
+    if (check_cfg(c) != SDV2_OK) return 0;
+    return static_cast<size_t>(c->batch) * c->heads * slots_of(c) * hw_of(c) * c->head_dim * 2;
+}
+
+size_t sdv2_meta_bytes(const sdv2_stream_cfg* c)
+{
+    if (check_cfg(c) != SDV2_OK) return 0;
+    return static_cast<size_t>(c->batch) * slots_of(c) * sizeof(sdv2_slot_meta);
+}
+
+int64_t sdv2_visible_tokens(const sdv2_stream_cfg* c, int64_t chunk_index)
+{
+    if (check_cfg(c) != SDV2_OK || chunk_index < 0) return -1;
+    return visible_frames(c, chunk_index) * hw_of(c);
+}
+
+sdv2_status sdv2_workspace_init(const sdv2_stream_cfg* c, void* ws, void* stream)
+{
+    sdv2_status s = check_cfg(c);
+    if (s != SDV2_OK) return s;
+    if (!ws || !aligned16(ws)) return fail(SDV2_ERR_INVALID_ARG, "ws must be a non-null 16-byte aligned pointer");
+    if ((s = check_device()) != SDV2_OK) return s;
+    const size_t bytes = sdv2_workspace_bytes(c);
+    std::vector<unsigned char> host(bytes, 0);
+    float* htab = reinterpret_cast<float*>(host.data() + kErrBytes);
+    const size_t hbytes = round_up(sizeof(float2) * c->grid_h * (c->rope_h / 2), 256);
+    float* wtab = reinterpret_cast<float*>(host.data() + kErrBytes + hbytes);
+    for (int y = 0; y < c->grid_h; ++y)
+        for (int j = 0; j < c->rope_h / 2; ++j) cos_sin_f32(y, j, c->rope_h, c->rope_base, htab + 2 * (y * (c->rope_h / 2) + j));
+    for (int x = 0; x < c->grid_w; ++x)
+        for (int j = 0; j < c->rope_w / 2; ++j) cos_sin_f32(x, j, c->rope_w, c->rope_base, wtab + 2 * (x * (c->rope_w / 2) + j));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(ws, host.data(), bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return cuda_status(e, "workspace upload");
+}
+
+sdv2_status sdv2_cache_reset(const sdv2_stream_cfg* c, void* k_cache, void* v_cache, void* meta, void* stream)
+{
+    sdv2_status s = check_cfg(c);
+    if (s != SDV2_OK) return s;
+    if (!k_cache || !v_cache || !meta || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(meta))
+        return fail(SDV2_ERR_INVALID_ARG, "k_cache, v_cache and meta must be non-null and 16-byte aligned");
+    if ((s = check_device()) != SDV2_OK) return s;
+    cudaError_t e = sdv2::launch_cache_reset(static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache),
+                                             sdv2_cache_bytes(c), static_cast<sdv2_slot_meta*>(meta),
+                                             static_cast<int64_t>(c->batch) * slots_of(c),
+                                             static_cast<cudaStream_t>(stream));
+    return cuda_status(e, "cache_reset launch");
+}
+
+sdv2_status sdv2_rope_append_kv(const sdv2_stream_cfg* c, const int64_t* start_frame, const int64_t* chunk_index,
+                                const void* q, const void* k, const void* v, void* q_rot, void* k_cache,
+                                void* v_cache, void* meta, void* ws, void* stream)
+{
+    sdv2_status s = check_cfg(c);
+    if (s != SDV2_OK) return s;
+    if (!start_frame || !chunk_index) return fail(SDV2_ERR_INVALID_ARG, "start_frame and chunk_index are required");
+    const void* ptrs[] = {q, k, v, q_rot, k_cache, v_cache, meta, ws};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return fail(SDV2_ERR_INVALID_ARG, "device pointers must be non-null and 16-byte aligned");
+    const int B = c->batch, F = c->chunk_frames, tp = c->rope_t / 2;
+    if (static_cast<int64_t>(B) * F > sdv2::kMaxChunkFrames || static_cast<int64_t>(B) * F * tp > sdv2::kMaxTimePairs)
+        return fail(SDV2_ERR_UNSUPPORTED, "B*F (%d) must be <= %d and B*F*rope_t/2 (%d) <= %d", B * F,
+                    sdv2::kMaxChunkFrames, B * F * tp, sdv2::kMaxTimePairs);
+    for (int b = 0; b < B; ++b) {
+        if (start_frame[b] < 0 || chunk_index[b] < 0)
+            return fail(SDV2_ERR_INVALID_ARG, "start_frame[%d] and chunk_index[%d] must be >= 0", b, b);
+        if (chunk_index[b] > (int64_t(1) << 40) || start_frame[b] > (int64_t(1) << 50))
+            return fail(SDV2_ERR_INVALID_ARG, "start_frame[%d] or chunk_index[%d] too large", b, b);
+    }
+    if ((s = check_device()) != SDV2_OK) return s;
+
+    static thread_local sdv2::RopeAppendParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int64_t hw = hw_of(c);
+    p.q = static_cast<const uint16_t*>(q);
+    p.k = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.q_rot = static_cast<uint16_t*>(q_rot);
+    p.k_cache = static_cast<uint16_t*>(k_cache);
+    p.v_cache = static_cast<uint16_t*>(v_cache);
+    p.meta = static_cast<sdv2_slot_meta*>(meta);
+    const size_t hbytes = round_up(sizeof(float2) * c->grid_h * (c->rope_h / 2), 256);
+    p.h_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + kErrBytes);
+    p.w_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + kErrBytes + hbytes);
+    p.tok_stride = c->qkv_token_stride ? c->qkv_token_stride : int64_t(c->heads) * c->head_dim;
+    p.B = B;
+    p.H = c->heads;
+    p.HW = static_cast<int32_t>(hw);
+    p.grid_w = c->grid_w;
+    p.F = F;
+    p.nslots = static_cast<int32_t>(slots_of(c));
+    p.Nq = static_cast<int32_t>(hw * F);
+    p.tp = tp;
+    p.hp = c->rope_h / 2;
+    p.wp = c->rope_w / 2;
+    for (int b = 0; b < B; ++b) {
+        const int64_t cidx = chunk_index[b];
+        const int64_t ceff = c->refresh_chunks > 0 ? cidx % c->refresh_chunks : cidx;
+        for (int i = 0; i < F; ++i) {
+            sdv2::FrameDesc& fd = p.frames[b * F + i];
+            fd.frame = cidx * F + i;
+            fd.tpos = start_frame[b] + ceff * F + i;
+            fd.slot = static_cast<int32_t>(slot_of(c, fd.frame));
+            for (int j = 0; j < tp; ++j) cos_sin_f32(fd.tpos, j, c->rope_t, c->rope_base, &p.tcs[(b * F + i) * tp + j].x);
+        }
+    }
+    return cuda_status(sdv2::launch_rope_append(p, static_cast<cudaStream_t>(stream)), "rope_append launch");
+}
+
+sdv2_status sdv2_chunk_attention(const sdv2_stream_cfg* c, const int64_t* chunk_index, const void* q_rot,
+                                 const void* k_cache, const void* v_cache, float scale, void* out, float* lse,
+                                 void* ws, void* stream)
+{
+    sdv2_status s = check_cfg(c);
+    if (s != SDV2_OK) return s;
+    if (!chunk_index) return fail(SDV2_ERR_INVALID_ARG, "chunk_index is required");
+    const void* ptrs[] = {q_rot, k_cache, v_cache, out, ws};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return fail(SDV2_ERR_INVALID_ARG, "device pointers must be non-null and 16-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(SDV2_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    if (c->batch > sdv2::kMaxAttnStreams)
+        return fail(SDV2_ERR_UNSUPPORTED, "batch (%d) > %d streams per attention call", c->batch, sdv2::kMaxAttnStreams);
+    if (static_cast<int64_t>(c->heads) * c->batch > 65535) return fail(SDV2_ERR_UNSUPPORTED, "too many heads");
+    if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(c->head_dim));
+    if (!std::isfinite(scale)) return fail(SDV2_ERR_INVALID_ARG, "scale must be finite");
+    int32_t nkv[sdv2::kMaxAttnStreams];
+    for (int b = 0; b < c->batch; ++b) {
+        if (chunk_index[b] < 0) return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be >= 0", b);
+        nkv[b] = static_cast<int32_t>(visible_frames(c, chunk_index[b]) * hw_of(c));
+    }
+    if ((s = check_device()) != SDV2_OK) return s;
+    const char* why = "launch";
+    cudaError_t e = sdv2::launch_chunk_attention(
+        static_cast<const uint16_t*>(q_rot), static_cast<const uint16_t*>(k_cache), static_cast<const uint16_t*>(v_cache),
+        c->batch, c->heads, static_cast<int>(hw_of(c) * c->chunk_frames), slots_of(c) * hw_of(c), nkv, scale,
+        static_cast<uint16_t*>(out), lse, static_cast<uint32_t*>(ws), g_timeout_ns.load(), g_drop_tile.load(),
+        static_cast<cudaStream_t>(stream), &why);
+    return cuda_status(e, why);
+}
+
+sdv2_status sdv2_motion_l2(const uint8_t* frames, int32_t B, int64_t T, int32_t Hp, int32_t Wp, int32_t C,
+                           uint64_t* ssd, float* m, void* stream)
+{
+    if (!frames || !ssd || !aligned16(frames) || !aligned16(ssd) || (m && !aligned16(m)))
+        return fail(SDV2_ERR_INVALID_ARG, "frames and ssd (and m if given) must be non-null and 16-byte aligned");
+    if (B < 1 || T < 1 || Hp < 1 || Wp < 1 || C < 1)
+        return fail(SDV2_ERR_INVALID_ARG, "B, T, Hp, Wp, C must be >= 1");
+    const int64_t npix = static_cast<int64_t>(Hp) * Wp * C;
+    if (npix % 16) return fail(SDV2_ERR_INVALID_ARG, "Hp*Wp*C (%lld) must be a multiple of 16", (long long)npix);
+    if (static_cast<int64_t>(B) * ((T + 31) / 32) > 65535)
+        return fail(SDV2_ERR_UNSUPPORTED, "B*ceil(T/32) must be <= 65535");
+    if (npix > (int64_t(1) << 40)) return fail(SDV2_ERR_INVALID_ARG, "frame too large");
+    sdv2_status s = check_device();
+    if (s != SDV2_OK) return s;
+    return cuda_status(sdv2::launch_motion_l2(frames, B, T, npix, ssd, m, static_cast<cudaStream_t>(stream)),
+                       "motion_l2 launch");
+}
+
+sdv2_status sdv2_check_device_error(void* ws, void* stream)
+{
+    if (!ws) return fail(SDV2_ERR_INVALID_ARG, "ws is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && word) e = cudaMemsetAsync(ws, 0, sizeof(word), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e, "check_device_error");
+    if (word & sdv2::kErrTimeout) return fail(SDV2_ERR_TIMEOUT, "a bounded device wait gave up (error word 0x%x)", word);
+    return ok();
+}
+
+}  // extern "C"

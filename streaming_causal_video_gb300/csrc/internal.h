@@ -1,0 +1,82 @@
+// Launch parameters and launchers shared by the library's translation units (not installed).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/sdv2.h"
+
+namespace sdv2 {
+
+// Bits of the device error word at the start of the workspace.
+constexpr uint32_t kErrTimeout = 1u;   // a bounded mbarrier wait gave up
+
+// ---- RoPE + cache append ----------------------------------------------------------------------
+
+constexpr int kMaxChunkFrames = 64;     // B*F frames per append call
+constexpr int kMaxTimePairs = 1536;     // B*F*(rope_t/2) fp32 cos/sin pairs per append call
+
+// Where one frame of the chunk goes: its cache slot, its stream-relative number and its RoPE
+// time index.  One entry per (stream b, frame i), index b*F + i.
+struct FrameDesc {
+    int64_t frame;
+    int64_t tpos;
+    int32_t slot;
+    int32_t pad;
+};
+
+struct RopeAppendParams {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    uint16_t* q_rot;
+    uint16_t* k_cache;
+    uint16_t* v_cache;
+    sdv2_slot_meta* meta;
+    const float2* h_tab;      // [grid_h][rope_h/2] (cos, sin)
+    const float2* w_tab;      // [grid_w][rope_w/2] (cos, sin)
+    int64_t tok_stride;       // elements between tokens of q/k/v
+    int32_t B, H, HW, grid_w, F, nslots, Nq;
+    int32_t tp, hp, wp;       // rotation pairs per axis
+    FrameDesc frames[kMaxChunkFrames];
+    float2 tcs[kMaxTimePairs];  // [B*F][tp] (cos, sin) of the time axis
+};
+
+cudaError_t launch_rope_append(const RopeAppendParams& p, cudaStream_t s);
+
+// ---- chunk attention --------------------------------------------------------------------------
+
+constexpr int kMaxAttnStreams = 16;
+
+struct AttnParams {
+    CUtensorMap qmap;                       // (D, Nq, B*H) over q_rot
+    CUtensorMap kmap[kMaxAttnStreams];      // per stream: (D, valid rows, H) over k_cache
+    CUtensorMap vmap[kMaxAttnStreams];      // per stream: (D, valid rows, H) over v_cache
+    uint16_t* out;                          // [B][Nq][H][D] bf16
+    float* lse;                             // [B][H][Nq] or null
+    uint32_t* err;                          // device error word
+    int32_t nkv[kMaxAttnStreams];           // valid rows per stream
+    int32_t B, H, Nq;
+    float scale_log2;                       // softmax scale * log2(e)
+    uint64_t timeout_ns;
+    int64_t drop_tile;                      // fault injection: KV tile whose copy is skipped, or -1
+};
+
+// Encodes the tensor maps and launches; returns the CUDA error of the launch.
+cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cache,
+                                   const uint16_t* v_cache, int B, int H, int Nq,
+                                   int64_t rows_per_head, const int32_t* nkv, float scale,
+                                   uint16_t* out, float* lse, uint32_t* err, uint64_t timeout_ns,
+                                   int64_t drop_tile, cudaStream_t s, const char** why);
+
+// ---- motion -----------------------------------------------------------------------------------
+
+cudaError_t launch_motion_l2(const uint8_t* frames, int B, int64_t T, int64_t frame_bytes,
+                             uint64_t* ssd, float* m, cudaStream_t s);
+
+// ---- misc kernels -----------------------------------------------------------------------------
+
+cudaError_t launch_cache_reset(uint16_t* k, uint16_t* v, size_t cache_bytes, sdv2_slot_meta* meta,
+                               int64_t nmeta, cudaStream_t s);
+
+}  // namespace sdv2

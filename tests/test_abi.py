@@ -1,0 +1,124 @@
+"""CPU tests of the C ABI: the library loads, exports what the header declares, and its host
+logic (sizes, visible prefix, argument validation) agrees with the oracle's list model.
+No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+import streaming_causal_video_gb300 as sd
+from synth_inputs import WORKLOADS, stream_config_dict
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build_library()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "sdv2.h")).read()
+    return sorted(set(re.findall(r"\b(sdv2_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    declared = header_functions()
+    assert len(declared) == 14, declared
+    L = sd.lib()
+    missing = [n for n in declared if not hasattr(L, n)]
+    assert not missing, missing
+    assert sorted(sd.exported_symbols()) == declared
+
+
+def test_config_struct_layout():
+    assert ctypes.sizeof(sd.StreamConfig) == 64
+    assert sd.StreamConfig.rope_base.offset == 24
+    assert sd.StreamConfig.qkv_token_stride.offset == 56
+
+
+def _cfg(name="tiny", **over):
+    d = stream_config_dict(WORKLOADS[name])
+    d.update(over)
+    return sd.StreamConfig.make(**d)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_sizes(name):
+    w = WORKLOADS[name]
+    c = _cfg(name)
+    assert sd.cache_bytes(c) == w.batch * w.heads * w.slots * w.hw * w.head_dim * 2
+    assert sd.meta_bytes(c) == w.batch * w.slots * 16
+    assert sd.workspace_bytes(c) >= 256 + (w.grid_h * 21 + w.grid_w * 21) * 8
+
+
+@pytest.mark.parametrize("F,Fs,W", [(3, 3, 4), (3, 3, 18), (3, 2, 3), (3, 0, 6), (2, 5, 2), (1, 1, 1)])
+def test_visible_tokens_equals_list_model(F, Fs, W):
+    c = _cfg(chunk_frames=F, sink_frames=Fs, window_frames=W)
+    cache = oracle.FrameListCache(Fs, W)
+    hw = c.grid_h * c.grid_w
+    for ch in range(40):
+        for i in range(F):
+            cache.append(ch * F + i, 0, None, None)
+        assert sd.visible_tokens(c, ch) == len(cache.frames()) * hw
+    assert sd.visible_tokens(c, -1) == -1
+
+
+def _status(fn, *args):
+    with pytest.raises(sd.SDV2Error) as e:
+        fn(*args)
+    return e.value.status
+
+
+FAKE = 1 << 20          # an aligned non-null address; every call below is rejected before use
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(rope_t=46), 1),                       # split does not sum to head_dim
+    (dict(rope_t=43, rope_h=43), 1),            # odd split
+    (dict(head_dim=64, rope_t=22, rope_h=22, rope_w=20), 2),   # not built
+    (dict(window_frames=2), 1),                 # window smaller than a chunk
+    (dict(sink_frames=-1), 1),
+    (dict(refresh_chunks=-2), 1),
+    (dict(rope_base=1.0), 1),
+    (dict(qkv_token_stride=12), 1),             # smaller than H*D
+    (dict(grid_h=0), 1),
+])
+def test_invalid_configs_are_rejected(over, status):
+    c = _cfg(**over)
+    assert sd.cache_bytes(c) == 0
+    assert _status(sd.rope_append_kv, c, [0], [0], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == status
+    assert _status(sd.chunk_attention, c, [0], FAKE, FAKE, FAKE, FAKE, FAKE, None, 0.0, 0) == status
+
+
+def test_invalid_pointers_and_indices_are_rejected():
+    c = _cfg()
+    assert _status(sd.rope_append_kv, c, [0], [0], FAKE + 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == 1
+    assert _status(sd.rope_append_kv, c, [0], [-1], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == 1
+    assert _status(sd.rope_append_kv, c, [-5], [0], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == 1
+    assert _status(sd.chunk_attention, c, [-1], FAKE, FAKE, FAKE, FAKE, FAKE, None, 0.0, 0) == 1
+    assert _status(sd.chunk_attention, c, [0], 0, FAKE, FAKE, FAKE, FAKE, None, 0.0, 0) == 1
+    big = _cfg(batch=17)
+    assert _status(sd.chunk_attention, big, [0] * 17, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0.0, 0) == 2
+    wide = _cfg(batch=30)     # 30 streams x 3 frames > 64 frames per append call
+    assert _status(sd.rope_append_kv, wide, [0] * 30, [0] * 30, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                   FAKE, 0) == 2
+
+
+def test_motion_argument_checks():
+    L = sd.lib()
+    assert L.sdv2_motion_l2(FAKE, 1, 1, 3, 5, 1, FAKE, None, None) == 1        # 15 bytes per frame
+    assert b"multiple of 16" in L.sdv2_last_error()
+    assert L.sdv2_motion_l2(FAKE, 1, 0, 4, 4, 1, FAKE, None, None) == 1        # T = 0
+    assert L.sdv2_motion_l2(FAKE + 4, 1, 1, 4, 4, 1, FAKE, None, None) == 1    # misaligned
+    assert L.sdv2_motion_l2(None, 1, 1, 4, 4, 1, FAKE, None, None) == 1
+    assert L.sdv2_motion_l2(FAKE, 1 << 16, 64, 4, 4, 1, FAKE, None, None) == 2  # grid too tall
+
+
+def test_status_strings():
+    L = sd.lib()
+    assert L.sdv2_status_string(0) == b"ok"
+    assert L.sdv2_status_string(4) == b"device wait timed out"
