@@ -383,7 +383,8 @@ def run_ours(args, dist):
                             % (w.layers, 2 * sd.cache_bytes(cfg) * w.layers / 1e9),
                       "step": "1 chunk: motion over %d video frames + %d denoise steps x %d layers x "
                               "(rope_append_kv + chunk_attention) at steady state (Nkv=%d)"
-                              % (vf, w.denoise_steps, w.layers, w.slots * w.hw)},
+                              % (vf, w.denoise_steps, w.layers, w.slots * w.hw),
+                      "kv_splits": sd.last_kv_splits()},
            "latent_frames_per_s": round(latent_fps, 3),
            "pct_bf16_peak": round(100.0 * value / peak, 2),
            "gpu_launches": launches_per_step * args.steps,

@@ -87,8 +87,12 @@ typedef struct {
 
 /* ---- sizes ------------------------------------------------------------------------------ */
 
-/* Bytes of the workspace: RoPE tables for the h and w axes plus a device error word.  The
- * workspace belongs to one configuration; it may be shared by all layers and both calls. */
+/* Bytes of the workspace: a header with the device error word, the fp32 cos/sin tables of the
+ * h and w axes, and the attention's key-split scratch (per-item arrival counters, per-row
+ * running max and sum, per-row unnormalised fp32 outputs for up to 4 key splits of every
+ * (stream, head, 256 query rows) item).  The workspace belongs to one configuration; it may
+ * be shared by all layers, but calls that use it must not overlap on the GPU (use one
+ * workspace per concurrently running stream). */
 size_t sdv2_workspace_bytes(const sdv2_stream_cfg* cfg);
 
 /* Bytes of ONE of the two cache tensors (k or v) of one layer:
@@ -104,9 +108,10 @@ int64_t sdv2_visible_tokens(const sdv2_stream_cfg* cfg, int64_t chunk_index);
 
 /* ---- set-up ----------------------------------------------------------------------------- */
 
-/* Fill the workspace: fp32 cos/sin tables of the h and w axes (angles and cos/sin in fp64 on
- * the host, rounded once to fp32) and a cleared error word.  Enqueues copies on `stream` and
- * synchronizes it before returning.  ws: device, sdv2_workspace_bytes(cfg) bytes. */
+/* Fill the workspace: zero it, then write the header and the fp32 cos/sin tables of the h and
+ * w axes (angles and cos/sin in fp64 on the host, rounded once to fp32).  Enqueues a memset
+ * and copies on `stream` and synchronizes it before returning.
+ * ws: device, sdv2_workspace_bytes(cfg) bytes. */
 sdv2_status sdv2_workspace_init(const sdv2_stream_cfg* cfg, void* ws, void* stream);
 
 /* Make one layer's cache empty: every slot's frame_id = -1, tpos = 0, and k and v zero.
@@ -152,8 +157,11 @@ sdv2_status sdv2_rope_append_kv(const sdv2_stream_cfg* cfg, const int64_t* start
  * scale: softmax scale; <= 0 selects 1/sqrt(D).
  * out: device bf16 [B][Nq][H][D] (token-major, ready for the output projection).
  * lse: device fp32 [B][H][Nq] natural-log log-sum-exp of the scaled scores, or NULL.
- * ws: device workspace (holds the error word of the bounded waits).
+ * ws: device workspace (error word of the bounded waits; key-split scratch).
  * Numerics: bf16 tensor-core products with fp32 accumulation, online softmax in fp32.
+ * Work split: one CTA per (stream, head, 256 query rows, key split); the key range of an item
+ * is cut into 1-4 splits chosen to fill whole waves of the GPU's SMs; the split that finishes
+ * last merges the others' partial rows (log-sum-exp weights) and writes the output.
  * Limits: B <= 16; the device must be sm_103 (tcgen05 tensor cores).
  */
 sdv2_status sdv2_chunk_attention(const sdv2_stream_cfg* cfg, const int64_t* chunk_index,
@@ -175,9 +183,10 @@ sdv2_status sdv2_motion_l2(const uint8_t* frames, int32_t B, int64_t T, int32_t 
 
 /* ---- errors ----------------------------------------------------------------------------- */
 
-/* Synchronizes `stream`, reads and clears the workspace's device error word, and returns
- * SDV2_ERR_TIMEOUT if a bounded device wait gave up since the last check (the outputs of the
- * calls involved are then undefined), SDV2_ERR_CUDA on a CUDA error, else SDV2_OK. */
+/* Synchronizes `stream`, reads the workspace's device error word and returns SDV2_ERR_TIMEOUT
+ * if a bounded device wait gave up since the last check (the outputs of the calls involved
+ * are then undefined), SDV2_ERR_CUDA on a CUDA error, else SDV2_OK.  After an error it clears
+ * the error word and the key-split counters, so the workspace is usable again. */
 sdv2_status sdv2_check_device_error(void* ws, void* stream);
 
 /* Upper bound of every bounded device-side wait, in nanoseconds (default 2e9).  Applies to
@@ -188,6 +197,13 @@ void sdv2_set_wait_timeout_ns(uint64_t ns);
  * sdv2_chunk_attention launches skip the copy of KV tile `tile` (the consumers' waits then
  * run out, the kernel records SDV2_ERR_TIMEOUT and returns).  -1 turns it off. */
 void sdv2_debug_drop_kv_tile(int64_t tile);
+
+/* Key-range split count of later sdv2_chunk_attention calls: 0 = automatic (default),
+ * 1..4 = forced (capped by the number of key tiles).  For tests and tuning. */
+void sdv2_debug_set_kv_splits(int32_t splits);
+
+/* Split count used by this thread's most recent sdv2_chunk_attention call. */
+int32_t sdv2_last_kv_splits(void);
 
 const char* sdv2_status_string(sdv2_status s);
 const char* sdv2_last_error(void);

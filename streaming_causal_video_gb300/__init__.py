@@ -13,6 +13,8 @@ from ._binding import (  # noqa: F401
     check_device_error,
     chunk_attention,
     debug_drop_kv_tile,
+    debug_set_kv_splits,
+    last_kv_splits,
     exported_symbols,
     lib,
     lib_path,

@@ -14,7 +14,8 @@ STATUS_NAMES = {0: "SDV2_OK", 1: "SDV2_ERR_INVALID_ARG", 2: "SDV2_ERR_UNSUPPORTE
 EXPORTS = ["sdv2_workspace_bytes", "sdv2_cache_bytes", "sdv2_meta_bytes", "sdv2_visible_tokens",
            "sdv2_workspace_init", "sdv2_cache_reset", "sdv2_rope_append_kv", "sdv2_chunk_attention",
            "sdv2_motion_l2", "sdv2_check_device_error", "sdv2_set_wait_timeout_ns",
-           "sdv2_debug_drop_kv_tile", "sdv2_status_string", "sdv2_last_error"]
+           "sdv2_debug_drop_kv_tile", "sdv2_debug_set_kv_splits", "sdv2_last_kv_splits",
+           "sdv2_status_string", "sdv2_last_error"]
 
 
 class SDV2Error(RuntimeError):
@@ -88,6 +89,10 @@ def lib():
         L.sdv2_set_wait_timeout_ns.argtypes = [u64]
         L.sdv2_debug_drop_kv_tile.restype = None
         L.sdv2_debug_drop_kv_tile.argtypes = [i64]
+        L.sdv2_debug_set_kv_splits.restype = None
+        L.sdv2_debug_set_kv_splits.argtypes = [i32]
+        L.sdv2_last_kv_splits.restype = i32
+        L.sdv2_last_kv_splits.argtypes = []
         L.sdv2_status_string.restype = ctypes.c_char_p
         L.sdv2_status_string.argtypes = [ctypes.c_int]
         L.sdv2_last_error.restype = ctypes.c_char_p
@@ -186,3 +191,11 @@ def set_wait_timeout_ns(ns: int):
 
 def debug_drop_kv_tile(tile: int):
     lib().sdv2_debug_drop_kv_tile(int(tile))
+
+
+def debug_set_kv_splits(n: int):
+    lib().sdv2_debug_set_kv_splits(int(n))
+
+
+def last_kv_splits() -> int:
+    return lib().sdv2_last_kv_splits()

@@ -31,7 +31,9 @@
 // frees its tensor memory before returning.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <atomic>
+#include <cmath>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -52,6 +54,7 @@ constexpr int MMA_WARP = 4 * NQT + 1;
 constexpr int NTHREADS = (4 * NQT + 2) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
 
 // barrier indices
 constexpr int B_QFULL = 0;
@@ -77,6 +80,11 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, uint32_t* 
     atomicOr(err, kErrTimeout);
 }
 
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -94,15 +102,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
     const uint32_t bar0 = smem_u32(bars);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 #define BAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
 
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
     const int lane = threadIdx.x & 31;
+    const int qp = blockIdx.x / p.splits;           // query pair (256 rows)
+    const int sp = blockIdx.x - qp * p.splits;      // key-range split
     const int h = blockIdx.y;
     const int b = blockIdx.z;
     const int nkv = p.nkv[b];
-    const int ntiles = (nkv + BN - 1) / BN;
-    const int q0 = blockIdx.x * (BM * NQT);
+    const int tiles_all = (nkv + BN - 1) / BN;
+    const int t_begin = static_cast<int>(static_cast<int64_t>(sp) * tiles_all / p.splits);
+    const int ntiles = static_cast<int>(static_cast<int64_t>(sp + 1) * tiles_all / p.splits) - t_begin;
+    const int q0 = qp * (BM * NQT);
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -147,20 +160,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                 const int ks = j % KST;
                 const uint32_t kph = static_cast<uint32_t>(j / KST) & 1u;
                 if (!mbar_wait_bounded(BAR(B_KEMPTY + ks), kph ^ 1u, tmo, abort_flag)) { raise_abort(abort_flag, p.err); break; }
-                if (j != p.drop_tile) {
+                const int jg = t_begin + j;
+                if (jg != p.drop_tile) {
                     mbar_arrive_expect_tx(BAR(B_KFULL + ks), TILE);
                     for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d(sK + ks * TILE + hf * HALF, km, BAR(B_KFULL + ks), hf * 64, j * BN, h);
+                        tma_load_3d(sK + ks * TILE + hf * HALF, km, BAR(B_KFULL + ks), hf * 64, jg * BN, h);
                     kpend[ks] = 1;
                     kpar[ks] = kph;
                 }
                 const int vs = j % VST;
                 const uint32_t vph = static_cast<uint32_t>(j / VST) & 1u;
                 if (!mbar_wait_bounded(BAR(B_VEMPTY + vs), vph ^ 1u, tmo, abort_flag)) { raise_abort(abort_flag, p.err); break; }
-                if (j != p.drop_tile) {
+                if (jg != p.drop_tile) {
                     mbar_arrive_expect_tx(BAR(B_VFULL + vs), TILE);
                     for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d(sV + vs * TILE + hf * HALF, vm, BAR(B_VFULL + vs), hf * 64, j * BN, h);
+                        tma_load_3d(sV + vs * TILE + hf * HALF, vm, BAR(B_VFULL + vs), hf * 64, jg * BN, h);
                     vpend[vs] = 1;
                     vpar[vs] = vph;
                 }
@@ -255,16 +269,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
             tc_fence_after();
             uint32_t r[128];
             tmem_ld_x128_sync(tS, r);
-            const int valid = min(BN, nkv - j * BN);
-            float mx = -INFINITY;
+            const int valid = nkv - (t_begin + j) * BN;      // > 0; < BN only on the last tile
+            if (valid < BN) {
 #pragma unroll
-            for (int i = 0; i < 128; ++i) {
-                float x = __uint_as_float(r[i]) * sl2;
-                if (i >= valid) x = -INFINITY;
-                r[i] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+                for (int i = 0; i < 128; ++i)
+                    if (i >= valid) r[i] = 0xFF800000u;       // -inf: masked key
             }
-            const float m_new = fmaxf(m_run, mx);
+            // Row max of the raw scores, 8 independent chains (scale > 0 commutes with max).
+            float mx8[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(r[a]);
+#pragma unroll
+            for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(r[i]));
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float m_new = fmaxf(m_run, mx * sl2);
             const bool grow = m_new > m_run + kRescaleThreshold;
             if (__any_sync(0xffffffffu, grow)) {
                 const float f = grow ? ex2_approx(m_run - m_new) : 1.0f;
@@ -284,52 +303,135 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                     m_run = m_new;
                 }
             }
-            float sum = 0.f;
+            // p = 2^(s * scale * log2(e) - m): one FFMA and one MUFU.EX2 per score.
+            const float neg_m = -m_run;
+            float sum8[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) sum8[a] = 0.f;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2_approx(__uint_as_float(r[hf * 64 + 2 * i]) - m_run);
-                    const float p1 = ex2_approx(__uint_as_float(r[hf * 64 + 2 * i + 1]) - m_run);
-                    sum += p0 + p1;
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(r[hf * 64 + 2 * i]), sl2, neg_m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(r[hf * 64 + 2 * i + 1]), sl2, neg_m));
+                    sum8[(2 * i) & 7] += p0;
+                    sum8[(2 * i + 1) & 7] += p1;
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st_x32(tS + hf * 32, pk);
             }
-            l_run += sum;
+            l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR(B_PFULL + t));
         }
-        if (!ok) {
-            raise_abort(abort_flag, p.err);
-        } else if (mbar_wait_bounded(BAR(B_OFULL + t), 0, tmo, abort_flag)) {
-            tc_fence_after();
-            const int q = q0 + t * BM + row;
-            const float inv = 1.0f / l_run;
-            uint16_t* dst = p.out + ((static_cast<int64_t>(b) * p.Nq + q) * p.H + h) * HD;
+        const int rloc = t * BM + row;                       // row inside the CTA's 256
+        const int q = q0 + rloc;
+        const int64_t item = (static_cast<int64_t>(b) * p.H + h) * p.qpairs + qp;
+        if (ok && !mbar_wait_bounded(BAR(B_OFULL + t), 0, tmo, abort_flag)) ok = false;
+        if (!ok) raise_abort(abort_flag, p.err);
+        if (ok) tc_fence_after();
+        if (p.splits == 1) {
+            if (ok) {
+                const float inv = 1.0f / l_run;
+                uint16_t* dst = p.out + ((static_cast<int64_t>(b) * p.Nq + q) * p.H + h) * HD;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t o[32];
-                tmem_ld_x32_sync(tO + c * 32, o);
-                if (q < p.Nq) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_x32_sync(tO + c * 32, o);
+                    if (q < p.Nq) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                        d4[v] = w;
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                            d4[v] = w;
+                        }
                     }
                 }
+                if (p.lse && q < p.Nq)
+                    p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + q] = (m_run + __log2f(l_run)) * kLn2;
             }
-            if (p.lse && q < p.Nq)
-                p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + q] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
         } else {
-            raise_abort(abort_flag, p.err);
+            // Split keys: publish this split's unnormalised rows, then the last split to arrive
+            // for this item merges all of them (no CTA waits for another).
+            const int64_t slot = (item * p.splits + sp) * kAttnRowsPerCta + rloc;
+            if (ok) {
+                float4* po = reinterpret_cast<float4*>(p.part_o + slot * HD);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld_x32_sync(tO + c * 32, o);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        __stcg(po + c * 8 + v, make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                                           __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
+                }
+                __stcg(reinterpret_cast<float2*>(p.part_ml) + slot, make_float2(m_run, l_run));
+            }
+            __threadfence();
+            named_bar_sync(1, 32 * 4 * NQT);
+            if (threadIdx.x == 0) {
+                int last = 0;
+                if (!*abort_flag) {
+                    const int prev = atomicAdd(p.counters + item, 1);
+                    last = (prev == p.splits - 1);
+                    if (last) p.counters[item] = 0;          // ready for the next call
+                }
+                *last_flag = last;
+            }
+            named_bar_sync(1, 32 * 4 * NQT);
+            if (*last_flag) {
+                __threadfence();
+                float ms[kMaxKvSplits], ls[kMaxKvSplits];
+                float M = -INFINITY;
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxKvSplits; ++s2) {
+                    if (s2 < p.splits) {
+                        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) +
+                                                 (item * p.splits + s2) * kAttnRowsPerCta + rloc);
+                        ms[s2] = ml.x;
+                        ls[s2] = ml.y;
+                        M = fmaxf(M, ml.x);
+                    }
+                }
+                float L = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxKvSplits; ++s2)
+                    if (s2 < p.splits) {
+                        ms[s2] = ex2_approx(ms[s2] - M);          // weight of split s2
+                        L += ls[s2] * ms[s2];
+                    }
+                const float inv = 1.0f / L;
+                if (q < p.Nq) {
+                    uint16_t* dst = p.out + ((static_cast<int64_t>(b) * p.Nq + q) * p.H + h) * HD;
+#pragma unroll 1
+                    for (int c = 0; c < HD / 8; ++c) {
+                        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int s2 = 0; s2 < kMaxKvSplits; ++s2) {
+                            if (s2 < p.splits) {
+                                const float4* src = reinterpret_cast<const float4*>(
+                                    p.part_o + ((item * p.splits + s2) * kAttnRowsPerCta + rloc) * HD + c * 8);
+                                const float4 u = __ldcg(src), w2 = __ldcg(src + 1);
+                                acc[0] += u.x * ms[s2]; acc[1] += u.y * ms[s2]; acc[2] += u.z * ms[s2]; acc[3] += u.w * ms[s2];
+                                acc[4] += w2.x * ms[s2]; acc[5] += w2.y * ms[s2]; acc[6] += w2.z * ms[s2]; acc[7] += w2.w * ms[s2];
+                            }
+                        }
+                        uint4 wv;
+                        wv.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+                        wv.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+                        wv.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+                        wv.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+                        *reinterpret_cast<uint4*>(dst + c * 8) = wv;
+                    }
+                    if (p.lse) p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + q] = (M + __log2f(L)) * kLn2;
+                }
+            }
         }
     }
 
@@ -379,16 +481,33 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t p
 
 }  // namespace
 
+int choose_kv_splits(int64_t items, int min_tiles, int slots)
+{
+    int best = 1;
+    double best_t = 1e300;
+    for (int sp = 1; sp <= kMaxKvSplits && sp <= min_tiles; ++sp) {
+        const double waves = std::ceil(static_cast<double>(items) * sp / slots);
+        const double t = waves / sp * (sp > 1 ? 1.02 : 1.0);   // 2 %: partial write + merge
+        if (t < best_t - 1e-9) {
+            best_t = t;
+            best = sp;
+        }
+    }
+    return best;
+}
+
 cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cache, const uint16_t* v_cache, int B,
                                    int H, int Nq, int64_t rows_per_head, const int32_t* nkv, float scale,
-                                   uint16_t* out, float* lse, uint32_t* err, uint64_t timeout_ns, int64_t drop_tile,
-                                   cudaStream_t s, const char** why)
+                                   uint16_t* out, float* lse, const AttnScratch& ws, uint64_t timeout_ns,
+                                   int64_t drop_tile, int force_splits, cudaStream_t s, int* splits_used,
+                                   const char** why)
 {
-    AttnParams p{};   // about 4.3 KB; passed by value as the launch's parameter block
+    AttnParams p{};   // about 4.4 KB; passed by value as the launch's parameter block
     if (!encode_rows_map(&p.qmap, q_rot, Nq, static_cast<int64_t>(B) * H, static_cast<int64_t>(Nq) * HD * 2)) {
         *why = "cuTensorMapEncodeTiled failed for q_rot";
         return cudaErrorInvalidValue;
     }
+    int min_tiles = 1 << 30;
     for (int b = 0; b < B; ++b) {
         const int64_t off = static_cast<int64_t>(b) * H * rows_per_head * HD;
         if (!encode_rows_map(&p.kmap[b], k_cache + off, nkv[b], H, rows_per_head * HD * 2) ||
@@ -397,10 +516,22 @@ cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cach
             return cudaErrorInvalidValue;
         }
         p.nkv[b] = nkv[b];
+        min_tiles = std::min(min_tiles, (nkv[b] + BN - 1) / BN);
     }
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    p.qpairs = (Nq + kAttnRowsPerCta - 1) / kAttnRowsPerCta;
+    const int64_t items = static_cast<int64_t>(B) * H * p.qpairs;
+    p.splits = force_splits > 0 ? std::min(force_splits, std::min(kMaxKvSplits, min_tiles))
+                                : choose_kv_splits(items, min_tiles, std::max(1, sms));
+    *splits_used = p.splits;
     p.out = out;
     p.lse = lse;
-    p.err = err;
+    p.err = ws.err;
+    p.counters = ws.counters;
+    p.part_ml = ws.part_ml;
+    p.part_o = ws.part_o;
     p.B = B;
     p.H = H;
     p.Nq = Nq;
@@ -409,8 +540,6 @@ cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cach
     p.drop_tile = drop_tile;
 
     static std::atomic<uint64_t> attr_set{0};   // one bit per device
-    int dev = 0;
-    cudaGetDevice(&dev);
     const uint64_t bit = uint64_t(1) << (dev & 63);
     if (!(attr_set.load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(chunk_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -421,8 +550,7 @@ cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cach
         }
         attr_set.fetch_or(bit);
     }
-    dim3 grid(static_cast<unsigned>((Nq + BM * NQT - 1) / (BM * NQT)), static_cast<unsigned>(H),
-              static_cast<unsigned>(B));
+    dim3 grid(static_cast<unsigned>(p.qpairs * p.splits), static_cast<unsigned>(H), static_cast<unsigned>(B));
     chunk_attention_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
     return cudaGetLastError();
 }

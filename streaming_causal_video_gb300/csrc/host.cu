@@ -23,7 +23,16 @@ thread_local char g_last_error[256] = "";
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int64_t> g_drop_tile{-1};
 
-constexpr size_t kErrBytes = 256;   // error word region at the start of the workspace
+constexpr size_t kErrBytes = 256;   // workspace header: error word and where the split counters are
+
+// First bytes of the workspace.  The error word is what the kernels set; the counter location
+// lets sdv2_check_device_error clear the split counters after an aborted launch.
+struct WsHeader {
+    uint32_t err;
+    uint32_t pad;
+    uint64_t counters_off;
+    uint64_t counters_bytes;
+};
 
 sdv2_status fail(sdv2_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 sdv2_status fail(sdv2_status s, const char* fmt, ...)
@@ -124,6 +133,36 @@ sdv2_status cuda_status(cudaError_t e, const char* what)
     return fail(SDV2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Workspace: [error word | h table | w table | split counters | split (m, l) | split rows].
+struct WsLayout {
+    size_t htab, wtab, counters, part_ml, part_o, total;
+};
+
+WsLayout ws_layout(const sdv2_stream_cfg* c)
+{
+    WsLayout L{};
+    const int64_t nq = hw_of(c) * c->chunk_frames;
+    const int64_t items = static_cast<int64_t>(c->batch) * c->heads *
+                          ((nq + sdv2::kAttnRowsPerCta - 1) / sdv2::kAttnRowsPerCta);
+    const int64_t rows = items * sdv2::kMaxKvSplits * sdv2::kAttnRowsPerCta;
+    size_t off = kErrBytes;
+    L.htab = off;
+    off += round_up(sizeof(float2) * c->grid_h * (c->rope_h / 2), 256);
+    L.wtab = off;
+    off += round_up(sizeof(float2) * c->grid_w * (c->rope_w / 2), 256);
+    L.counters = off;
+    off += round_up(sizeof(int32_t) * items, 256);
+    L.part_ml = off;
+    off += round_up(sizeof(float) * 2 * rows, 256);
+    L.part_o = off;
+    off += round_up(sizeof(float) * 128 * rows, 256);
+    L.total = off;
+    return L;
+}
+
+std::atomic<int> g_force_splits{0};
+thread_local int g_last_splits = 0;
+
 }  // namespace
 
 extern "C" {
@@ -146,11 +185,14 @@ void sdv2_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
 
 void sdv2_debug_drop_kv_tile(int64_t tile) { g_drop_tile.store(tile < 0 ? -1 : tile); }
 
+void sdv2_debug_set_kv_splits(int32_t splits) { g_force_splits.store(splits < 0 ? 0 : splits); }
+
+int32_t sdv2_last_kv_splits(void) { return g_last_splits; }
+
 size_t sdv2_workspace_bytes(const sdv2_stream_cfg* c)
 {
     if (check_cfg(c) != SDV2_OK) return 0;
-    return kErrBytes + round_up(sizeof(float2) * c->grid_h * (c->rope_h / 2), 256) +
-           round_up(sizeof(float2) * c->grid_w * (c->rope_w / 2), 256);
+    return ws_layout(c).total;
 }
 
 size_t sdv2_cache_bytes(const sdv2_stream_cfg* c)
@@ -177,17 +219,21 @@ sdv2_status sdv2_workspace_init(const sdv2_stream_cfg* c, void* ws, void* stream
     if (s != SDV2_OK) return s;
     if (!ws || !aligned16(ws)) return fail(SDV2_ERR_INVALID_ARG, "ws must be a non-null 16-byte aligned pointer");
     if ((s = check_device()) != SDV2_OK) return s;
-    const size_t bytes = sdv2_workspace_bytes(c);
-    std::vector<unsigned char> host(bytes, 0);
-    float* htab = reinterpret_cast<float*>(host.data() + kErrBytes);
-    const size_t hbytes = round_up(sizeof(float2) * c->grid_h * (c->rope_h / 2), 256);
-    float* wtab = reinterpret_cast<float*>(host.data() + kErrBytes + hbytes);
+    const WsLayout L = ws_layout(c);
+    std::vector<float> htab(2 * c->grid_h * (c->rope_h / 2)), wtab(2 * c->grid_w * (c->rope_w / 2));
     for (int y = 0; y < c->grid_h; ++y)
-        for (int j = 0; j < c->rope_h / 2; ++j) cos_sin_f32(y, j, c->rope_h, c->rope_base, htab + 2 * (y * (c->rope_h / 2) + j));
+        for (int j = 0; j < c->rope_h / 2; ++j) cos_sin_f32(y, j, c->rope_h, c->rope_base, &htab[2 * (y * (c->rope_h / 2) + j)]);
     for (int x = 0; x < c->grid_w; ++x)
-        for (int j = 0; j < c->rope_w / 2; ++j) cos_sin_f32(x, j, c->rope_w, c->rope_base, wtab + 2 * (x * (c->rope_w / 2) + j));
+        for (int j = 0; j < c->rope_w / 2; ++j) cos_sin_f32(x, j, c->rope_w, c->rope_base, &wtab[2 * (x * (c->rope_w / 2) + j)]);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpyAsync(ws, host.data(), bytes, cudaMemcpyHostToDevice, st);
+    unsigned char* base = static_cast<unsigned char*>(ws);
+    cudaError_t e = cudaMemsetAsync(ws, 0, L.total, st);
+    if (e == cudaSuccess && !htab.empty())
+        e = cudaMemcpyAsync(base + L.htab, htab.data(), htab.size() * sizeof(float), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && !wtab.empty())
+        e = cudaMemcpyAsync(base + L.wtab, wtab.data(), wtab.size() * sizeof(float), cudaMemcpyHostToDevice, st);
+    WsHeader hdr{0, 0, L.counters, L.part_ml - L.counters};
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ws, &hdr, sizeof(hdr), cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     return cuda_status(e, "workspace upload");
 }
@@ -238,9 +284,9 @@ sdv2_status sdv2_rope_append_kv(const sdv2_stream_cfg* c, const int64_t* start_f
     p.k_cache = static_cast<uint16_t*>(k_cache);
     p.v_cache = static_cast<uint16_t*>(v_cache);
     p.meta = static_cast<sdv2_slot_meta*>(meta);
-    const size_t hbytes = round_up(sizeof(float2) * c->grid_h * (c->rope_h / 2), 256);
-    p.h_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + kErrBytes);
-    p.w_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + kErrBytes + hbytes);
+    const WsLayout L = ws_layout(c);
+    p.h_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + L.htab);
+    p.w_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + L.wtab);
     p.tok_stride = c->qkv_token_stride ? c->qkv_token_stride : int64_t(c->heads) * c->head_dim;
     p.B = B;
     p.H = c->heads;
@@ -289,11 +335,15 @@ sdv2_status sdv2_chunk_attention(const sdv2_stream_cfg* c, const int64_t* chunk_
     }
     if ((s = check_device()) != SDV2_OK) return s;
     const char* why = "launch";
+    const WsLayout L = ws_layout(c);
+    unsigned char* base = static_cast<unsigned char*>(ws);
+    sdv2::AttnScratch scratch{reinterpret_cast<uint32_t*>(base), reinterpret_cast<int32_t*>(base + L.counters),
+                              reinterpret_cast<float*>(base + L.part_ml), reinterpret_cast<float*>(base + L.part_o)};
     cudaError_t e = sdv2::launch_chunk_attention(
         static_cast<const uint16_t*>(q_rot), static_cast<const uint16_t*>(k_cache), static_cast<const uint16_t*>(v_cache),
         c->batch, c->heads, static_cast<int>(hw_of(c) * c->chunk_frames), slots_of(c) * hw_of(c), nkv, scale,
-        static_cast<uint16_t*>(out), lse, static_cast<uint32_t*>(ws), g_timeout_ns.load(), g_drop_tile.load(),
-        static_cast<cudaStream_t>(stream), &why);
+        static_cast<uint16_t*>(out), lse, scratch, g_timeout_ns.load(), g_drop_tile.load(), g_force_splits.load(),
+        static_cast<cudaStream_t>(stream), &g_last_splits, &why);
     return cuda_status(e, why);
 }
 
@@ -319,13 +369,19 @@ sdv2_status sdv2_check_device_error(void* ws, void* stream)
 {
     if (!ws) return fail(SDV2_ERR_INVALID_ARG, "ws is NULL");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint32_t word = 0;
+    WsHeader hdr{};
     cudaError_t e = cudaStreamSynchronize(st);
-    if (e == cudaSuccess) e = cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess && word) e = cudaMemsetAsync(ws, 0, sizeof(word), st);
+    if (e == cudaSuccess) e = cudaMemcpy(&hdr, ws, sizeof(hdr), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && hdr.err) {
+        // An aborted launch may leave split counters mid-count: clear them with the error word.
+        e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), st);
+        if (e == cudaSuccess && hdr.counters_bytes)
+            e = cudaMemsetAsync(static_cast<unsigned char*>(ws) + hdr.counters_off, 0, hdr.counters_bytes, st);
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_status(e, "check_device_error");
-    if (word & sdv2::kErrTimeout) return fail(SDV2_ERR_TIMEOUT, "a bounded device wait gave up (error word 0x%x)", word);
+    if (hdr.err & sdv2::kErrTimeout)
+        return fail(SDV2_ERR_TIMEOUT, "a bounded device wait gave up (error word 0x%x)", hdr.err);
     return ok();
 }
 

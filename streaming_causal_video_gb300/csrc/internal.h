@@ -47,6 +47,8 @@ cudaError_t launch_rope_append(const RopeAppendParams& p, cudaStream_t s);
 // ---- chunk attention --------------------------------------------------------------------------
 
 constexpr int kMaxAttnStreams = 16;
+constexpr int kAttnRowsPerCta = 256;     // two 128-row query tiles per CTA
+constexpr int kMaxKvSplits = 4;          // key-range splits per (stream, head, query pair)
 
 struct AttnParams {
     CUtensorMap qmap;                       // (D, Nq, B*H) over q_rot
@@ -55,19 +57,39 @@ struct AttnParams {
     uint16_t* out;                          // [B][Nq][H][D] bf16
     float* lse;                             // [B][H][Nq] or null
     uint32_t* err;                          // device error word
+    int32_t* counters;                      // [B*H*qpairs] split arrivals (0 between calls)
+    float* part_ml;                         // [items*splits][256][2] running max (log2) and sum
+    float* part_o;                          // [items*splits][256][128] unnormalised output
     int32_t nkv[kMaxAttnStreams];           // valid rows per stream
     int32_t B, H, Nq;
+    int32_t qpairs;                         // ceil(Nq / 256)
+    int32_t splits;                         // key-range splits per item (1..kMaxKvSplits)
     float scale_log2;                       // softmax scale * log2(e)
     uint64_t timeout_ns;
     int64_t drop_tile;                      // fault injection: KV tile whose copy is skipped, or -1
 };
 
 // Encodes the tensor maps and launches; returns the CUDA error of the launch.
+// Workspace pieces used by the attention call.
+struct AttnScratch {
+    uint32_t* err;
+    int32_t* counters;
+    float* part_ml;
+    float* part_o;
+};
+
+// Encodes the tensor maps, picks the key-range split count (0 = automatic) and launches;
+// returns the CUDA error of the launch.  *splits_used receives the split count.
 cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cache,
                                    const uint16_t* v_cache, int B, int H, int Nq,
                                    int64_t rows_per_head, const int32_t* nkv, float scale,
-                                   uint16_t* out, float* lse, uint32_t* err, uint64_t timeout_ns,
-                                   int64_t drop_tile, cudaStream_t s, const char** why);
+                                   uint16_t* out, float* lse, const AttnScratch& ws,
+                                   uint64_t timeout_ns, int64_t drop_tile, int force_splits,
+                                   cudaStream_t s, int* splits_used, const char** why);
+
+// Split count that fills whole waves of `slots` CTAs best for `items` work items whose key
+// loops have at least `min_tiles` tiles (ties go to fewer splits).
+int choose_kv_splits(int64_t items, int min_tiles, int slots);
 
 // ---- motion -----------------------------------------------------------------------------------
 

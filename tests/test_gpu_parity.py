@@ -215,6 +215,29 @@ def test_repeated_call_is_deterministic():
     sd.check_device_error(sess.ws)
 
 
+@pytest.mark.parametrize("chunk_stop", [3, 8])
+def test_forced_kv_splits_all_match_oracle(chunk_stop):
+    """The same cached state attended with 1, 2, 3 and 4 key splits (the split that finishes
+    last merges the others' partial rows): every result matches the oracle."""
+    w = small_workload(WORKLOADS["wan13b_480p"], heads=2, grid_h=10, grid_w=16, chunks=chunk_stop)
+    ls = LockStep(w)
+    for c in range(chunk_stop):
+        q_rot_o = ls.step([c])
+    rows = sample_rows(w.nq, 48, 11)
+    try:
+        for splits in (1, 2, 3, 4):
+            sd.debug_set_kv_splits(splits)
+            L = ls.sess.layers[0]
+            sd.chunk_attention(ls.cfg, [chunk_stop - 1], ls.sess.q_rot, L.k, L.v, ls.sess.out, ls.sess.ws,
+                               lse=ls.lse)
+            torch.cuda.synchronize()
+            assert sd.last_kv_splits() == splits
+            ls.check_attention(q_rot_o, rows=rows)
+        sd.check_device_error(ls.sess.ws)
+    finally:
+        sd.debug_set_kv_splits(0)
+
+
 # ------------------------------------------------------------------------------------------
 # full workload shapes, in the launch configuration the bench times (sampled rows)
 # ------------------------------------------------------------------------------------------
