@@ -169,6 +169,38 @@ sdv2_status sdv2_chunk_attention(const sdv2_stream_cfg* cfg, const int64_t* chun
                                  float scale, void* out, float* lse, void* ws, void* stream);
 
 /*
+ * Chunk attention for callers that cannot allocate device memory.  (The pages describe no
+ * counterpart: this is an interface for deployment, not a step of the method.)
+ *
+ * Some callers cannot call cudaMalloc at all: code running inside a memory pool it does not
+ * own, plugin hosts that forbid allocation after start-up, real-time loops that must never
+ * reach the allocator (an allocation can synchronize the device and stall a frame).  They
+ * cannot provide the workspace sdv2_chunk_attention needs.  This entry point computes the same
+ * attention with the same arguments minus `ws`; its scratch (device error word, key-split
+ * arrival counters, per-row partial results of the key splits) lives in a 16 MiB file-scope
+ * __device__ array inside the library, which every GPU that loads the library holds until the
+ * process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *   with that device current) and keeps it; make that first call before any stream capture.
+ * - Every call on a device shares the array, which keeps the previous call's contents; each
+ *   call clears the error word and counters on `stream` (a memset) before its kernel.  Calls
+ *   whose work overlaps on the GPU (other streams, graph branches) race on the array: do not
+ *   overlap them.
+ * - Key splits are chosen as for sdv2_chunk_attention, then reduced until their partial rows
+ *   fit in the array (results stay within the same tolerance; speed may differ).
+ * - Sizes beyond the array's reach are rejected with SDV2_ERR_UNSUPPORTED before anything is
+ *   enqueued: batch * heads * ceil(Nq / 256) must be <= 16384.  Bounded device waits use the
+ *   default 2 s limit; a timeout leaves the outputs undefined and is not reported here (use
+ *   sdv2_chunk_attention with a workspace and sdv2_check_device_error to observe it).
+ * Other arguments, layouts and numerics: as sdv2_chunk_attention.
+ */
+sdv2_status sdv2_chunk_attention_noalloc(const sdv2_stream_cfg* cfg, const int64_t* chunk_index,
+                                         const void* q_rot, const void* k_cache,
+                                         const void* v_cache, float scale, void* out, float* lse,
+                                         void* stream);
+
+/*
  * Motion magnitude of adjacent frames ("StreamDiffusionV2" review page, section 二 table and
  * section 三: L2 motion estimation between adjacent frames feeds the noise controller).
  *

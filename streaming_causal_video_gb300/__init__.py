@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     cache_reset,
     check_device_error,
     chunk_attention,
+    chunk_attention_noalloc,
     debug_drop_kv_tile,
     debug_set_kv_splits,
     last_kv_splits,

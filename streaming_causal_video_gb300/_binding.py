@@ -13,6 +13,7 @@ STATUS_NAMES = {0: "SDV2_OK", 1: "SDV2_ERR_INVALID_ARG", 2: "SDV2_ERR_UNSUPPORTE
 # Every symbol that include/sdv2.h declares.
 EXPORTS = ["sdv2_workspace_bytes", "sdv2_cache_bytes", "sdv2_meta_bytes", "sdv2_visible_tokens",
            "sdv2_workspace_init", "sdv2_cache_reset", "sdv2_rope_append_kv", "sdv2_chunk_attention",
+           "sdv2_chunk_attention_noalloc",
            "sdv2_motion_l2", "sdv2_check_device_error", "sdv2_set_wait_timeout_ns",
            "sdv2_debug_drop_kv_tile", "sdv2_debug_set_kv_splits", "sdv2_last_kv_splits",
            "sdv2_status_string", "sdv2_last_error"]
@@ -81,6 +82,8 @@ def lib():
         L.sdv2_rope_append_kv.argtypes = [cfgp, i64p, i64p, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.sdv2_chunk_attention.restype = ctypes.c_int
         L.sdv2_chunk_attention.argtypes = [cfgp, i64p, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
+        L.sdv2_chunk_attention_noalloc.restype = ctypes.c_int
+        L.sdv2_chunk_attention_noalloc.argtypes = [cfgp, i64p, vp, vp, vp, ctypes.c_float, vp, vp, vp]
         L.sdv2_motion_l2.restype = ctypes.c_int
         L.sdv2_motion_l2.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp, vp]
         L.sdv2_check_device_error.restype = ctypes.c_int
@@ -172,6 +175,13 @@ def chunk_attention(cfg, chunk_index, q_rot, k_cache, v_cache, out, ws, lse=None
     _check(lib().sdv2_chunk_attention(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch), _ptr(q_rot),
                                       _ptr(k_cache), _ptr(v_cache), float(scale), _ptr(out), _ptr(lse), _ptr(ws),
                                       _stream(stream)), "sdv2_chunk_attention")
+
+
+def chunk_attention_noalloc(cfg, chunk_index, q_rot, k_cache, v_cache, out, lse=None, scale=0.0, stream=None):
+    """sdv2_chunk_attention_noalloc: the same attention without a caller-owned workspace."""
+    _check(lib().sdv2_chunk_attention_noalloc(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch), _ptr(q_rot),
+                                              _ptr(k_cache), _ptr(v_cache), float(scale), _ptr(out), _ptr(lse),
+                                              _stream(stream)), "sdv2_chunk_attention_noalloc")
 
 
 def motion_l2(frames, ssd, m=None, stream=None):

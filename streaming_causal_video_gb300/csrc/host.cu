@@ -165,6 +165,10 @@ thread_local int g_last_splits = 0;
 
 }  // namespace
 
+namespace sdv2 {
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg ? msg : ""); }
+}  // namespace sdv2
+
 extern "C" {
 
 const char* sdv2_status_string(sdv2_status s)

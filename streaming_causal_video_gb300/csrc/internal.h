@@ -96,6 +96,9 @@ int choose_kv_splits(int64_t items, int min_tiles, int slots);
 cudaError_t launch_motion_l2(const uint8_t* frames, int B, int64_t T, int64_t frame_bytes,
                              uint64_t* ssd, float* m, cudaStream_t s);
 
+// Sets the per-thread message returned by sdv2_last_error().
+void set_last_error(const char* msg);
+
 // ---- misc kernels -----------------------------------------------------------------------------
 
 cudaError_t launch_cache_reset(uint16_t* k, uint16_t* v, size_t cache_bytes, sdv2_slot_meta* meta,

@@ -1,0 +1,126 @@
+// sdv2_chunk_attention_noalloc: chunk attention for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at all -- for example code that runs inside a memory pool
+// it does not own, a plugin host that forbids allocation after start-up, or a real-time loop
+// that must never hit the allocator (an allocation can synchronize the device and stall a
+// frame).  Such callers cannot size and own the workspace that sdv2_chunk_attention needs.
+// This variant keeps its scratch (device error word, key-split arrival counters and the
+// per-row partial results of the key splits) in one file-scope __device__ array instead.
+//
+// The array is part of the library's module: every GPU that loads the library holds its
+// kNoAllocScratchBytes until the process exits.  All calls on a device share it, and it keeps
+// the previous call's contents; each call therefore clears the error word and the counters on
+// its stream before the kernel runs.  Calls whose kernels overlap on the GPU (different
+// streams, or graph branches) race on the array and must not be issued.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "internal.h"
+
+namespace sdv2 {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB per GPU
+constexpr size_t kNaHeader = 256;                            // error word
+constexpr int64_t kNaMaxItems = 16384;                       // (stream, head, 256 rows) items
+constexpr size_t kNaCounters = kNaHeader;
+constexpr size_t kNaCountersBytes = sizeof(int32_t) * kNaMaxItems;
+constexpr size_t kNaPartMl = kNaCounters + kNaCountersBytes;
+// Rows of split partials that fit: 8 bytes of (max, sum) + 512 bytes of output per row,
+// rounded down to whole 256-row units.
+constexpr int64_t kNaRows =
+    static_cast<int64_t>((kNoAllocScratchBytes - kNaPartMl - 256) / (8 + 512)) / kAttnRowsPerCta * kAttnRowsPerCta;
+constexpr size_t kNaPartO = kNaPartMl + ((static_cast<size_t>(kNaRows) * 8 + 255) / 256) * 256;
+static_assert(kNaPartO + static_cast<size_t>(kNaRows) * 512 <= kNoAllocScratchBytes, "no-alloc scratch layout");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_na_mutex;
+unsigned char* g_na_ptr[64] = {};          // device address of the array, per device
+
+sdv2_status na_fail(sdv2_status s, const char* msg)
+{
+    char buf[256];
+    snprintf(buf, sizeof(buf), "sdv2_chunk_attention_noalloc: %s", msg);
+    set_last_error(buf);     // readable through sdv2_last_error()
+    return s;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace sdv2
+
+extern "C" sdv2_status sdv2_chunk_attention_noalloc(const sdv2_stream_cfg* cfg, const int64_t* chunk_index,
+                                                    const void* q_rot, const void* k_cache, const void* v_cache,
+                                                    float scale, void* out, float* lse, void* stream)
+{
+    using namespace sdv2;
+    // Configuration and sizes (the library's own checks run inside these size queries).
+    if (!cfg || sdv2_cache_bytes(cfg) == 0) return na_fail(SDV2_ERR_INVALID_ARG, "invalid stream configuration");
+    if (!chunk_index) return na_fail(SDV2_ERR_INVALID_ARG, "chunk_index is required");
+    const void* ptrs[] = {q_rot, k_cache, v_cache, out};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return na_fail(SDV2_ERR_INVALID_ARG, "device pointers must be non-null and 16-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return na_fail(SDV2_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    if (cfg->batch > kMaxAttnStreams) return na_fail(SDV2_ERR_UNSUPPORTED, "more than 16 streams");
+    const int64_t hw = static_cast<int64_t>(cfg->grid_h) * cfg->grid_w;
+    const int nq = static_cast<int>(hw * cfg->chunk_frames);
+    const int64_t qpairs = (nq + kAttnRowsPerCta - 1) / kAttnRowsPerCta;
+    const int64_t items = static_cast<int64_t>(cfg->batch) * cfg->heads * qpairs;
+    if (items > kNaMaxItems)
+        return na_fail(SDV2_ERR_UNSUPPORTED,
+                       "batch * heads * ceil(Nq/256) exceeds 16384, the size its 16 MiB static scratch serves");
+    if (static_cast<int64_t>(cfg->heads) * cfg->batch > 65535) return na_fail(SDV2_ERR_UNSUPPORTED, "too many heads");
+    int32_t nkv[kMaxAttnStreams];
+    int min_tiles = 1 << 30;
+    for (int b = 0; b < cfg->batch; ++b) {
+        if (chunk_index[b] < 0) return na_fail(SDV2_ERR_INVALID_ARG, "chunk_index must be >= 0");
+        nkv[b] = static_cast<int32_t>(sdv2_visible_tokens(cfg, chunk_index[b]));
+        min_tiles = std::min(min_tiles, (nkv[b] + 127) / 128);
+    }
+    if (!(scale > 0.f)) scale = 1.0f / std::sqrt(static_cast<float>(cfg->head_dim));
+    if (!std::isfinite(scale)) return na_fail(SDV2_ERR_INVALID_ARG, "scale must be finite");
+
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return na_fail(SDV2_ERR_CUDA, "cudaGetDevice failed");
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) return na_fail(SDV2_ERR_UNSUPPORTED, "the library is built for sm_103a (GB300) only");
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+
+    // Set-up, once per device and with that device current: the device address of the array.
+    unsigned char* base;
+    {
+        std::lock_guard<std::mutex> lock(g_na_mutex);
+        if (!g_na_ptr[dev]) {
+            void* p = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess || !p) return na_fail(SDV2_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+            g_na_ptr[dev] = static_cast<unsigned char*>(p);
+        }
+        base = g_na_ptr[dev];
+    }
+
+    // Key splits: the automatic choice, reduced until its partial rows fit in the array.
+    int splits = choose_kv_splits(items, min_tiles, std::max(1, sms));
+    while (splits > 1 && items * splits * kAttnRowsPerCta > kNaRows) --splits;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's contents: clear the error word and the counters.
+    cudaError_t e = cudaMemsetAsync(base, 0, kNaPartMl, st);
+    if (e != cudaSuccess) return na_fail(SDV2_ERR_CUDA, "clearing the static scratch failed");
+    AttnScratch scratch{reinterpret_cast<uint32_t*>(base), reinterpret_cast<int32_t*>(base + kNaCounters),
+                        reinterpret_cast<float*>(base + kNaPartMl), reinterpret_cast<float*>(base + kNaPartO)};
+    int used = 0;
+    const char* why = "launch";
+    e = launch_chunk_attention(static_cast<const uint16_t*>(q_rot), static_cast<const uint16_t*>(k_cache),
+                               static_cast<const uint16_t*>(v_cache), cfg->batch, cfg->heads, nq,
+                               (static_cast<int64_t>(cfg->sink_frames) + cfg->window_frames) * hw, nkv, scale,
+                               static_cast<uint16_t*>(out), lse, scratch, 2000000000ull, -1, splits, st, &used, &why);
+    if (e != cudaSuccess) return na_fail(SDV2_ERR_CUDA, why);
+    set_last_error("");
+    return SDV2_OK;
+}
