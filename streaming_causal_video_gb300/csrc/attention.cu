@@ -8,10 +8,11 @@
 // caching; "StreamDiffusionV2" review page, section 三: sink tokens + rolling KV cache).
 //   out[b, n, h, :] = sum_j softmax_j(scale * q_rot[b, h, n, :] . k[b, h, j, :]) v[b, h, j, :]
 //
-// How (one CTA = one head of one stream and two 128-row query tiles):
-//   warp 8 (TMA)      : Q tiles once, then K and V tiles of 128 keys through 2-stage rings.
-//                       3D tensor maps per stream clip the key range at the valid prefix, so
-//                       rows past it arrive as zeros; 128-byte swizzled boxes of 64 dims.
+// How (one CTA = one head of one stream, two 128-row query tiles and one key split):
+//   warps 8, 10 (TMA): Q tiles once, then K (warp 8) and V (warp 10) tiles of 128 keys through
+//                       2-stage rings, each prefetched into L2 four tiles ahead.  3D tensor
+//                       maps per stream clip the key range at the valid prefix, so rows past it
+//                       arrive as zeros; 128-byte swizzled boxes of 64 dims.
 //   warp 9 (MMA)      : one thread issues tcgen05.mma.  S_t = Q_t K^T (A and B from shared
 //                       memory, K-major) into tensor memory; O_t += P_t V (A = P from tensor
 //                       memory, B = V from shared memory, MN-major).  Completion is signalled
@@ -49,9 +50,11 @@ constexpr int KST = 2;                  // K stages
 constexpr int VST = 2;                  // V stages
 constexpr uint32_t TILE = BM * HD * 2;  // 32 KB
 constexpr uint32_t HALF = TILE / 2;     // one 64-dim box: 128 rows x 128 bytes
-constexpr int TMA_WARP = 4 * NQT;
-constexpr int MMA_WARP = 4 * NQT + 1;
-constexpr int NTHREADS = (4 * NQT + 2) * 32;
+constexpr int TMA_WARP = 4 * NQT;        // Q and K tiles
+constexpr int MMA_WARP = 4 * NQT + 1;    // MMA issue (also allocates tensor memory)
+constexpr int TMA_V_WARP = 4 * NQT + 2;  // V tiles
+constexpr int NTHREADS = (4 * NQT + 3) * 32;
+constexpr int PREFETCH_TILES = 4;        // K/V tiles prefetched into L2 ahead of their load
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
@@ -140,52 +143,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == TMA_WARP) {
-        // ------------------------------------------------------------------ producer (TMA)
+    if (warp == TMA_WARP || warp == TMA_V_WARP) {
+        // ------------------------------------------------------------------ producers (TMA)
+        // One thread loads Q and the K ring, another the V ring, so that a late K slot never
+        // holds back a V load.  Each also prefetches its tiles PREFETCH_TILES ahead into L2:
+        // the CTAs of one head walk the same keys in step, so without it every tile would be a
+        // DRAM-latency load.
         if (lane == 0) {
-            const CUtensorMap* qm = &p.qmap;
-            const CUtensorMap* km = &p.kmap[b];
-            const CUtensorMap* vm = &p.vmap[b];
-            tma_prefetch_desc(qm);
-            tma_prefetch_desc(km);
-            tma_prefetch_desc(vm);
-            const int plane = b * p.H + h;
-            mbar_arrive_expect_tx(BAR(B_QFULL), NQT * TILE);
-            for (int t = 0; t < NQT; ++t)
-                for (int hf = 0; hf < 2; ++hf)
-                    tma_load_3d(sQ + t * TILE + hf * HALF, qm, BAR(B_QFULL), hf * 64, q0 + t * BM, plane);
-            int kpend[KST] = {}, vpend[VST] = {};
-            uint32_t kpar[KST] = {}, vpar[VST] = {};
+            const bool is_k = (warp == TMA_WARP);
+            const CUtensorMap* map = is_k ? &p.kmap[b] : &p.vmap[b];
+            tma_prefetch_desc(map);
+            const uint32_t s_ring = is_k ? sK : sV;
+            const int bar_full = is_k ? B_KFULL : B_VFULL;
+            const int bar_empty = is_k ? B_KEMPTY : B_VEMPTY;
+            constexpr int NST = KST;                 // KST == VST
+            static_assert(KST == VST, "one ring depth for K and V");
+            if (is_k) {
+                const CUtensorMap* qm = &p.qmap;
+                tma_prefetch_desc(qm);
+                const int plane = b * p.H + h;
+                mbar_arrive_expect_tx(BAR(B_QFULL), NQT * TILE);
+                for (int t = 0; t < NQT; ++t)
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d(sQ + t * TILE + hf * HALF, qm, BAR(B_QFULL), hf * 64, q0 + t * BM, plane);
+            }
+            for (int j = 0; j < PREFETCH_TILES && j < ntiles; ++j)
+                for (int hf = 0; hf < 2; ++hf) tma_prefetch_l2_3d(map, hf * 64, (t_begin + j) * BN, h);
+            int pend[NST] = {};
+            uint32_t par[NST] = {};
             for (int j = 0; j < ntiles; ++j) {
-                const int ks = j % KST;
-                const uint32_t kph = static_cast<uint32_t>(j / KST) & 1u;
-                if (!mbar_wait_bounded(BAR(B_KEMPTY + ks), kph ^ 1u, tmo, abort_flag)) { raise_abort(abort_flag, p.err); break; }
+                const int st = j % NST;
+                const uint32_t ph = static_cast<uint32_t>(j / NST) & 1u;
+                if (!mbar_wait_bounded(BAR(bar_empty + st), ph ^ 1u, tmo, abort_flag)) { raise_abort(abort_flag, p.err); break; }
                 const int jg = t_begin + j;
+                if (j + PREFETCH_TILES < ntiles)
+                    for (int hf = 0; hf < 2; ++hf) tma_prefetch_l2_3d(map, hf * 64, (jg + PREFETCH_TILES) * BN, h);
                 if (jg != p.drop_tile) {
-                    mbar_arrive_expect_tx(BAR(B_KFULL + ks), TILE);
+                    mbar_arrive_expect_tx(BAR(bar_full + st), TILE);
                     for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d(sK + ks * TILE + hf * HALF, km, BAR(B_KFULL + ks), hf * 64, jg * BN, h);
-                    kpend[ks] = 1;
-                    kpar[ks] = kph;
-                }
-                const int vs = j % VST;
-                const uint32_t vph = static_cast<uint32_t>(j / VST) & 1u;
-                if (!mbar_wait_bounded(BAR(B_VEMPTY + vs), vph ^ 1u, tmo, abort_flag)) { raise_abort(abort_flag, p.err); break; }
-                if (jg != p.drop_tile) {
-                    mbar_arrive_expect_tx(BAR(B_VFULL + vs), TILE);
-                    for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d(sV + vs * TILE + hf * HALF, vm, BAR(B_VFULL + vs), hf * 64, jg * BN, h);
-                    vpend[vs] = 1;
-                    vpar[vs] = vph;
+                        tma_load_3d(s_ring + st * TILE + hf * HALF, map, BAR(bar_full + st), hf * 64, jg * BN, h);
+                    pend[st] = 1;
+                    par[st] = ph;
                 }
             }
             // Drain: every copy this thread started must land before the CTA may exit.
             volatile int no_abort = 0;
-            mbar_wait_bounded(BAR(B_QFULL), 0, tmo, &no_abort);
-            for (int i = 0; i < KST; ++i)
-                if (kpend[i]) mbar_wait_bounded(BAR(B_KFULL + i), kpar[i], tmo, &no_abort);
-            for (int i = 0; i < VST; ++i)
-                if (vpend[i]) mbar_wait_bounded(BAR(B_VFULL + i), vpar[i], tmo, &no_abort);
+            if (is_k) mbar_wait_bounded(BAR(B_QFULL), 0, tmo, &no_abort);
+            for (int i = 0; i < NST; ++i)
+                if (pend[i]) mbar_wait_bounded(BAR(bar_full + i), par[i], tmo, &no_abort);
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
