@@ -13,10 +13,13 @@
 //                       2-stage rings, each prefetched into L2 four tiles ahead.  3D tensor
 //                       maps per stream clip the key range at the valid prefix, so rows past it
 //                       arrive as zeros; 128-byte swizzled boxes of 64 dims.
-//   warp 9 (MMA)      : one thread issues tcgen05.mma.  S_t = Q_t K^T (A and B from shared
-//                       memory, K-major) into tensor memory; O_t += P_t V (A = P from tensor
-//                       memory, B = V from shared memory, MN-major).  Completion is signalled
-//                       with tcgen05.commit on mbarriers.
+//   warp 9 (MMA)      : runs converged; an elected lane issues each tcgen05.mma.  S_t = Q_t K^T
+//                       (A and B from shared memory, K-major) into tensor memory;
+//                       O_t += P_t V (A = P from tensor memory, B = V from shared memory,
+//                       MN-major).  Completion is signalled with tcgen05.commit on mbarriers.
+//                       Descriptors are built once and advanced by constants, because the
+//                       issuing warp's own instruction latency between MMAs, not the tensor core,
+//                       is what limits a single MMA stream of 128x128x16 steps.
 //   warps 0-3, 4-7    : one softmax warpgroup per query tile; thread = query row = TMEM lane.
 //                       Online softmax in fp32 with a lazily updated running max (the output
 //                       accumulator in tensor memory is rescaled only when the max grows by more
@@ -195,64 +198,75 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t idO = idesc_bf16_f32(BM, HD, true);
-            auto issue_s = [&](int t, int ks) {
+        // The whole warp runs this loop converged; lane 0 does the barrier waits and broadcasts
+        // the outcome, one elected lane issues each tcgen05 instruction.  Shared-memory
+        // descriptors are built once: the k-th 16-wide step of a K-major 128-byte-swizzled tile
+        // starts (k/4)*HALF + (k%4)*32 bytes further, and V's k-th step 16 rows (2048 bytes)
+        // further, which is a constant added to the descriptor's address field.
+        constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false);
+        constexpr uint32_t idO = idesc_bf16_f32(BM, HD, true);
+        const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+        const uint64_t dK = sdesc_sw128(sK, 16, 1024);
+        const uint64_t dV = sdesc_sw128(sV, HALF, 1024);
+        constexpr uint64_t kTileStep = TILE >> 4;           // descriptor units (16 bytes)
+        auto wait = [&](int bar_idx, uint32_t parity) -> bool {
+            int r = 1;
+            if (lane == 0) r = mbar_wait_bounded(BAR(bar_idx), parity, tmo, abort_flag) ? 1 : 0;
+            return __shfl_sync(0xffffffffu, r, 0) != 0;
+        };
+        auto issue_s = [&](int t, int ks) {
+            const uint64_t a0 = dQ + static_cast<uint64_t>(t) * kTileStep;
+            const uint64_t b0 = dK + static_cast<uint64_t>(ks) * kTileStep;
 #pragma unroll
-                for (int k = 0; k < HD / 16; ++k) {
-                    const uint32_t off = static_cast<uint32_t>(k >> 2) * HALF + static_cast<uint32_t>(k & 3) * 32u;
-                    const uint64_t a = sdesc_sw128(sQ + t * TILE + off, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(sK + ks * TILE + off, 16, 1024);
-                    mma_ss(tmem + s_col(t), a, bd, idS, k > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int t, int vs, bool acc) {
+            for (int k = 0; k < HD / 16; ++k) {
+                const uint64_t o = static_cast<uint64_t>(((k >> 2) * HALF + (k & 3) * 32) >> 4);
+                mma_ss_warp(tmem + s_col(t), a0 + o, b0 + o, idS, k > 0 ? 1u : 0u);
+            }
+        };
+        auto issue_pv = [&](int t, int vs, bool acc) {
+            const uint64_t b0 = dV + static_cast<uint64_t>(vs) * kTileStep;
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const uint64_t bd = sdesc_sw128(sV + vs * TILE + static_cast<uint32_t>(k) * 2048u, HALF, 1024);
-                    mma_ts(tmem + o_col(t), tmem + s_col(t) + static_cast<uint32_t>(k) * 8u, bd, idO,
-                           (acc || k > 0) ? 1u : 0u);
-                }
-            };
-            bool ok = mbar_wait_bounded(BAR(B_QFULL), 0, tmo, abort_flag) &&
-                      mbar_wait_bounded(BAR(B_KFULL + 0), 0, tmo, abort_flag);
-            if (ok) {
+            for (int k = 0; k < BN / 16; ++k)
+                mma_ts_warp(tmem + o_col(t), tmem + s_col(t) + static_cast<uint32_t>(k) * 8u,
+                            b0 + static_cast<uint64_t>(k) * (2048u >> 4), idO, (acc || k > 0) ? 1u : 0u);
+        };
+        bool ok = wait(B_QFULL, 0) && wait(B_KFULL + 0, 0);
+        if (ok) {
+            tc_fence_after();
+            for (int t = 0; t < NQT; ++t) {
+                issue_s(t, 0);
+                mma_commit_warp(BAR(B_SFULL + t));
+            }
+            mma_commit_warp(BAR(B_KEMPTY + 0));
+        }
+        for (int j = 0; ok && j < ntiles; ++j) {
+            const int vs = j % VST;
+            if (!wait(B_VFULL + vs, static_cast<uint32_t>(j / VST) & 1u)) { ok = false; break; }
+            const bool more = j + 1 < ntiles;
+            const int ks = (j + 1) % KST;
+            for (int t = 0; t < NQT; ++t) {
+                if (!wait(B_PFULL + t, static_cast<uint32_t>(j) & 1u)) { ok = false; break; }
                 tc_fence_after();
-                for (int t = 0; t < NQT; ++t) {
-                    issue_s(t, 0);
-                    mma_commit(BAR(B_SFULL + t));
-                }
-                mma_commit(BAR(B_KEMPTY + 0));
-            }
-            for (int j = 0; ok && j < ntiles; ++j) {
-                const int vs = j % VST;
-                if (!mbar_wait_bounded(BAR(B_VFULL + vs), static_cast<uint32_t>(j / VST) & 1u, tmo, abort_flag)) { ok = false; break; }
-                const bool more = j + 1 < ntiles;
-                const int ks = (j + 1) % KST;
-                for (int t = 0; t < NQT; ++t) {
-                    if (!mbar_wait_bounded(BAR(B_PFULL + t), static_cast<uint32_t>(j) & 1u, tmo, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_pv(t, vs, j > 0);
-                    if (!more) mma_commit(BAR(B_OFULL + t));
-                    if (more) {
-                        if (t == 0 &&
-                            !mbar_wait_bounded(BAR(B_KFULL + ks), static_cast<uint32_t>((j + 1) / KST) & 1u, tmo, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_s(t, ks);
-                        mma_commit(BAR(B_SFULL + t));
+                issue_pv(t, vs, j > 0);
+                if (!more) mma_commit_warp(BAR(B_OFULL + t));
+                if (more) {
+                    if (t == 0 && !wait(B_KFULL + ks, static_cast<uint32_t>((j + 1) / KST) & 1u)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    issue_s(t, ks);
+                    mma_commit_warp(BAR(B_SFULL + t));
                 }
-                if (!ok) break;
-                mma_commit(BAR(B_VEMPTY + vs));
-                if (more) mma_commit(BAR(B_KEMPTY + ks));
             }
-            if (!ok) raise_abort(abort_flag, p.err);
-            // Drain: all MMAs issued by this thread complete before tensor memory is freed.
-            mma_commit(BAR(B_MMADONE));
+            if (!ok) break;
+            mma_commit_warp(BAR(B_VEMPTY + vs));
+            if (more) mma_commit_warp(BAR(B_KEMPTY + ks));
+        }
+        if (!ok && lane == 0) raise_abort(abort_flag, p.err);
+        // Drain: all MMAs issued by this warp complete before tensor memory is freed.
+        mma_commit_warp(BAR(B_MMADONE));
+        if (lane == 0) {
             volatile int no_abort = 0;
             mbar_wait_bounded(BAR(B_MMADONE), 0, tmo, &no_abort);
         }
