@@ -9,8 +9,8 @@
 //   out[b, n, h, :] = sum_j softmax_j(scale * q_rot[b, h, n, :] . k[b, h, j, :]) v[b, h, j, :]
 //
 // How (one CTA = one head of one stream, two 128-row query tiles and one key split):
-//   warps 8, 10 (TMA): Q tiles once, then K (warp 8) and V (warp 10) tiles of 128 keys through
-//                       2-stage rings, each prefetched into L2 four tiles ahead.  3D tensor
+//   warps 8, 10 (TMA): Q tiles once, then K (warp 8, 3-stage ring) and V (warp 10, 2-stage ring)
+//                       tiles of 128 keys, each prefetched into L2 four tiles ahead.  3D tensor
 //                       maps per stream clip the key range at the valid prefix, so rows past it
 //                       arrive as zeros; 128-byte swizzled boxes of 64 dims.
 //   warp 9 (MMA)      : runs converged; an elected lane issues each tcgen05.mma.  S_t = Q_t K^T
@@ -49,7 +49,7 @@ constexpr int BM = 128;                 // query rows per tile
 constexpr int BN = 128;                 // keys per KV tile
 constexpr int HD = 128;                 // head dim
 constexpr int NQT = 2;                  // query tiles per CTA
-constexpr int KST = 2;                  // K stages
+constexpr int KST = 3;                  // K stages
 constexpr int VST = 2;                  // V stages
 constexpr uint32_t TILE = BM * HD * 2;  // 32 KB
 constexpr uint32_t HALF = TILE / 2;     // one 64-dim box: 128 rows x 128 bytes
@@ -159,8 +159,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
             const uint32_t s_ring = is_k ? sK : sV;
             const int bar_full = is_k ? B_KFULL : B_VFULL;
             const int bar_empty = is_k ? B_KEMPTY : B_VEMPTY;
-            constexpr int NST = KST;                 // KST == VST
-            static_assert(KST == VST, "one ring depth for K and V");
+            const int nst = is_k ? KST : VST;
+            constexpr int NST = KST > VST ? KST : VST;
             if (is_k) {
                 const CUtensorMap* qm = &p.qmap;
                 tma_prefetch_desc(qm);
@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
             int pend[NST] = {};
             uint32_t par[NST] = {};
             for (int j = 0; j < ntiles; ++j) {
-                const int st = j % NST;
-                const uint32_t ph = static_cast<uint32_t>(j / NST) & 1u;
+                const int st = j % nst;
+                const uint32_t ph = static_cast<uint32_t>(j / nst) & 1u;
                 if (!mbar_wait_bounded(BAR(bar_empty + st), ph ^ 1u, tmo, abort_flag)) { raise_abort(abort_flag, p.err); break; }
                 const int jg = t_begin + j;
                 if (j + PREFETCH_TILES < ntiles)
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
             // Drain: every copy this thread started must land before the CTA may exit.
             volatile int no_abort = 0;
             if (is_k) mbar_wait_bounded(BAR(B_QFULL), 0, tmo, &no_abort);
-            for (int i = 0; i < NST; ++i)
+            for (int i = 0; i < nst; ++i)
                 if (pend[i]) mbar_wait_bounded(BAR(bar_full + i), par[i], tmo, &no_abort);
         }
         __syncwarp();
@@ -294,14 +294,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                 for (int i = 0; i < 128; ++i)
                     if (i >= valid) r[i] = 0xFF800000u;       // -inf: masked key
             }
-            // Row max of the raw scores, 8 independent chains (scale > 0 commutes with max).
+            // Row max of the raw scores (scale > 0 commutes with max): 8 independent chains of
+            // three-input max, each over the 16 scores i = a (mod 8).
             float mx8[8];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(r[a]);
+            for (int a = 0; a < 8; ++a) {
+                float m = fmax3(__uint_as_float(r[a]), __uint_as_float(r[a + 8]), __uint_as_float(r[a + 16]));
 #pragma unroll
-            for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(r[i]));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int i = 24; i < 120; i += 16)
+                    m = fmax3(m, __uint_as_float(r[i + a]), __uint_as_float(r[i + 8 + a]));
+                mx8[a] = fmaxf(m, __uint_as_float(r[120 + a]));
+            }
+            const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
             const float m_new = fmaxf(m_run, mx * sl2);
             const bool grow = m_new > m_run + kRescaleThreshold;
             if (__any_sync(0xffffffffu, grow)) {
@@ -322,25 +326,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                     m_run = m_new;
                 }
             }
-            // p = 2^(s * scale * log2(e) - m): one FFMA and one MUFU.EX2 per score.
-            const float neg_m = -m_run;
-            float sum8[8];
+            // p = 2^(s * scale * log2(e) - m): one packed FFMA per two scores, one MUFU.EX2 per
+            // score; the row sum accumulates pairs with packed adds in 4 independent chains.
+            const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
+            const uint64_t negm2 = f32x2_pack(-m_run, -m_run);
+            uint64_t sum4[4];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) sum8[a] = 0.f;
+            for (int a = 0; a < 4; ++a) sum4[a] = 0;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(r[hf * 64 + 2 * i]), sl2, neg_m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(r[hf * 64 + 2 * i + 1]), sl2, neg_m));
-                    sum8[(2 * i) & 7] += p0;
-                    sum8[(2 * i + 1) & 7] += p1;
+                    const int e = hf * 64 + 2 * i;
+                    const uint64_t x = ffma2(f32x2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sl2x2, negm2);
+                    float x0, x1;
+                    f32x2_unpack(x, x0, x1);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    sum4[i & 3] = fadd2(sum4[i & 3], f32x2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st_x32(tS + hf * 32, pk);
             }
-            l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+            {
+                const uint64_t s01 = fadd2(sum4[0], sum4[1]), s23 = fadd2(sum4[2], sum4[3]);
+                float lo, hi;
+                f32x2_unpack(fadd2(s01, s23), lo, hi);
+                l_run += lo + hi;
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(BAR(B_PFULL + t));
