@@ -208,7 +208,7 @@ sdv2_status sdv2_chunk_attention_noalloc(const sdv2_stream_cfg* cfg, const int64
  * ssd: device uint64 [B][T]: ssd[b][t] = sum over pixels and channels of
  *   (frames[b][t+1] - frames[b][t])^2, exact.
  * m: device fp32 [B][T] or NULL: sqrt(ssd / (Hp*Wp*C)), the RMS pixel difference.
- * Requires T >= 1 and Hp*Wp*C a multiple of 16.
+ * Requires T >= 1, B*T <= 65535 and Hp*Wp*C a multiple of 16.
  */
 sdv2_status sdv2_motion_l2(const uint8_t* frames, int32_t B, int64_t T, int32_t Hp, int32_t Wp,
                            int32_t C, uint64_t* ssd, float* m, void* stream);

@@ -360,8 +360,8 @@ sdv2_status sdv2_motion_l2(const uint8_t* frames, int32_t B, int64_t T, int32_t 
         return fail(SDV2_ERR_INVALID_ARG, "B, T, Hp, Wp, C must be >= 1");
     const int64_t npix = static_cast<int64_t>(Hp) * Wp * C;
     if (npix % 16) return fail(SDV2_ERR_INVALID_ARG, "Hp*Wp*C (%lld) must be a multiple of 16", (long long)npix);
-    if (static_cast<int64_t>(B) * ((T + 31) / 32) > 65535)
-        return fail(SDV2_ERR_UNSUPPORTED, "B*ceil(T/32) must be <= 65535");
+    if (static_cast<int64_t>(B) * T > 65535)
+        return fail(SDV2_ERR_UNSUPPORTED, "B*T must be <= 65535");
     if (npix > (int64_t(1) << 40)) return fail(SDV2_ERR_INVALID_ARG, "frame too large");
     sdv2_status s = check_device();
     if (s != SDV2_OK) return s;

@@ -7,9 +7,11 @@
 //
 // Work split: each block owns a slab of 16-byte vectors of the frame and a run of consecutive
 // frame pairs; a thread keeps its vectors of frame t in registers while it reads frame t+1, so
-// every frame is read from HBM once per run.  Per pair: |a-b| per byte (vabsdiffu4) and the
+// every frame is read from HBM once per run (runs are as long as the grid size allows).  Per pair: |a-b| per byte (vabsdiffu4) and the
 // 4-way dot product with itself (dp4a) accumulate in 32 bits, then a block reduction and one
 // 64-bit atomic add per block and pair.
+#include <algorithm>
+
 #include "internal.h"
 
 namespace sdv2 {
@@ -17,7 +19,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVecPerThread = 4;
-constexpr int kFramesPerRun = 32;
+constexpr int kMaxFramesPerRun = 32;
 
 __device__ __forceinline__ uint32_t ssd16(uint4 a, uint4 b, uint32_t acc)
 {
@@ -35,15 +37,16 @@ __global__ void motion_zero_kernel(uint64_t* ssd, int64_t n)
     if (i < n) ssd[i] = 0;
 }
 
-// grid: x = slabs of kThreads*kVecPerThread vectors, y = stream * runs + run.
+// grid: x = slabs of kThreads*kVecPerThread vectors, y = stream * runs + run; a run covers
+// `fpr` consecutive frame pairs.
 __global__ void __launch_bounds__(kThreads) motion_ssd_kernel(const uint4* __restrict__ frames, int64_t vecs,
-                                                              int64_t T, int runs, uint64_t* __restrict__ ssd)
+                                                              int64_t T, int runs, int fpr, uint64_t* __restrict__ ssd)
 {
     const int b = blockIdx.y / runs;
     const int run = blockIdx.y - b * runs;
-    const int64_t t0 = static_cast<int64_t>(run) * kFramesPerRun;
+    const int64_t t0 = static_cast<int64_t>(run) * fpr;
     if (t0 >= T) return;
-    const int64_t t1 = min(T, t0 + kFramesPerRun);
+    const int64_t t1 = min(T, t0 + fpr);
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads * kVecPerThread + threadIdx.x;
     const uint4* f = frames + static_cast<int64_t>(b) * (T + 1) * vecs;
 
@@ -95,9 +98,16 @@ cudaError_t launch_motion_l2(const uint8_t* frames, int B, int64_t T, int64_t fr
     motion_zero_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(ssd, n);
     const int64_t vecs = frame_bytes / 16;
     const int64_t slabs = (vecs + kThreads * kVecPerThread - 1) / (kThreads * kVecPerThread);
-    const int runs = static_cast<int>((T + kFramesPerRun - 1) / kFramesPerRun);
+    // Frames per run: long runs read each frame once, short runs give more blocks; aim for at
+    // least four blocks per SM (a run's first frame is read twice, from L2 when runs are short).
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = static_cast<int64_t>(B) * slabs * T / (4 * static_cast<int64_t>(sms));
+    const int fpr = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxFramesPerRun, want)));
+    const int runs = static_cast<int>((T + fpr - 1) / fpr);
     dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(B * runs));
-    motion_ssd_kernel<<<grid, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(frames), vecs, T, runs, ssd);
+    motion_ssd_kernel<<<grid, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(frames), vecs, T, runs, fpr, ssd);
     if (m) {
         motion_rms_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(ssd, m, n,
                                                                                static_cast<double>(frame_bytes));

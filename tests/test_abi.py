@@ -115,7 +115,7 @@ def test_motion_argument_checks():
     assert L.sdv2_motion_l2(FAKE, 1, 0, 4, 4, 1, FAKE, None, None) == 1        # T = 0
     assert L.sdv2_motion_l2(FAKE + 4, 1, 1, 4, 4, 1, FAKE, None, None) == 1    # misaligned
     assert L.sdv2_motion_l2(None, 1, 1, 4, 4, 1, FAKE, None, None) == 1
-    assert L.sdv2_motion_l2(FAKE, 1 << 16, 64, 4, 4, 1, FAKE, None, None) == 2  # grid too tall
+    assert L.sdv2_motion_l2(FAKE, 1 << 10, 64, 4, 4, 1, FAKE, None, None) == 2  # B*T > 65535
 
 
 def test_status_strings():

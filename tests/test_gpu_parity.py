@@ -285,6 +285,7 @@ def test_stream_batch_full_shape_identical_streams_shift_invariance():
     (1, 33, 20, 24, 3),        # crosses a 32-frame run
     (3, 65, 16, 20, 3),
     (2, 20, 480, 832, 3),      # the 480p frame
+    (2, 140, 480, 832, 3),     # long runs of 32 frame pairs and a ragged last run
 ])
 def test_motion_exact(B, T, hp, wp, ch):
     frames = motion_frames_host(B, T + 1, hp, wp, ch, seed=B * 100 + T)
