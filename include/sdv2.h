@@ -213,6 +213,60 @@ sdv2_status sdv2_chunk_attention_noalloc(const sdv2_stream_cfg* cfg, const int64
 sdv2_status sdv2_motion_l2(const uint8_t* frames, int32_t B, int64_t T, int32_t Hp, int32_t Wp,
                            int32_t C, uint64_t* ssd, float* m, void* stream);
 
+/* ---- refresh, sink update, noise controller ------------------------------------------- */
+
+/*
+ * RoPE refresh, second reading ("StreamDiffusionV2" review page, section 三: the positional
+ * offset is reset periodically).  sdv2_rope_append_kv already restarts the time offset every R
+ * chunks (t = S + F*(c mod R) + i); the keys kept in the window were rotated at the old,
+ * larger positions.  This call turns them back by F*R on the time axis so that the distance
+ * between the new chunk and every window frame stays what it was without the reset.
+ *
+ * For every stream b whose chunk_index[b] is a refresh chunk (R > 0, c > 0, c mod R == 0):
+ * every WINDOW slot (slot >= F_s) holding a frame of an earlier chunk (0 <= frame_id < c*F)
+ * has the time-axis pairs of its keys rotated by the angle -F*R*omega_j (same rounding as
+ * sdv2_rope_append_kv, with position -F*R) and its tpos decreased by F*R.  Sink slots, values,
+ * the h/w dims and streams not at a refresh chunk are untouched.  Call it once per layer at a
+ * refresh chunk, BEFORE the chunk's first sdv2_rope_append_kv (not again for later denoise
+ * steps of the same chunk).
+ * k_cache: device [B][H][(F_s+W)*HW][D] bf16; meta: device [B][F_s+W]; chunk_index: host [B].
+ * Limits: B <= 64.
+ */
+sdv2_status sdv2_rope_refresh_rerotate(const sdv2_stream_cfg* cfg, const int64_t* chunk_index,
+                                       void* k_cache, void* meta, void* stream);
+
+/*
+ * Sink update ("StreamDiffusionV2" gist summary 2.A.2: sink tokens follow recent visual
+ * context).  Read here as: the sink is replaced by copies of the F_s most recently appended
+ * frames.  For every stream b with update[b] != 0 (host int32 [B]), after chunk chunk_index[b]
+ * has been appended (n = (c+1)*F frames), sink slot s (0 <= s < F_s) receives the k and v rows
+ * and the metadata (frame_id, tpos) of frame n - F_s + s, which lives in the window.  Needs
+ * n >= 2*F_s and W >= F_s.  The copies keep their rotation; the window keeps the originals.
+ */
+sdv2_status sdv2_sink_update(const sdv2_stream_cfg* cfg, const int64_t* chunk_index,
+                             const int32_t* update, void* k_cache, void* v_cache, void* meta,
+                             void* stream);
+
+/* Motion-aware noise controller: a declared monotone map (the pages give no formula and
+ * disagree on its direction: gist summary 2.A.3 vs review page section 三). */
+typedef struct {
+    float motion_lo, motion_hi;  /* RMS motion (0..255 scale) mapped to the low / high end     */
+    float rate_lo, rate_hi;      /* noise rates at the two ends (>= 0)                          */
+    float ema;                   /* smoothing over frames, in [0, 1); 0 = none                  */
+    int32_t more_noise_when_fast;/* 1: fast motion -> rate_hi (review page); 0: -> rate_lo      */
+} sdv2_noise_ctl;
+
+/*
+ * rate[b][t] from m[b][t] (device fp32 [B][T], e.g. the RMS output of sdv2_motion_l2):
+ *   u = clamp((m - motion_lo) / (motion_hi - motion_lo), 0, 1); if !more_noise_when_fast:
+ *   u = 1 - u; r = fmaf(rate_hi - rate_lo, u, rate_lo);
+ *   s = (first value of the stream) ? r : fmaf(ema, s - r, r);  rate[b][t] = s.
+ * state: device fp32 [B] carried across calls (-1 = no history yet) or NULL (no carry-over).
+ * fp32 throughout, one rounding per written operation (fmaf where written).
+ */
+sdv2_status sdv2_noise_from_motion(const sdv2_noise_ctl* ctl, const float* m, int32_t B, int64_t T,
+                                   float* state, float* rate, void* stream);
+
 /* ---- errors ----------------------------------------------------------------------------- */
 
 /* Synchronizes `stream`, reads the workspace's device error word and returns SDV2_ERR_TIMEOUT

@@ -20,6 +20,15 @@ What each function follows (pages are cited by title and section):
 * rope_spec / rope_ideal -- 3D RoPE over (t, h, w) segments (C code, see sdv2_oracle.c).
 * attention -- softmax(q k^T / sqrt(D)) v over every retained key, fp64.
 * motion_ssd -- squared L2 distance of adjacent frames, exact integers ("L2 运动估计").
+* StreamOracle.refresh_rerotate -- second reading of the RoPE refresh: at a refresh chunk the
+  window frames' keys are turned back by F*R on the time axis (rope_spec with positions
+  (-F*R, 0, 0)), and their time index decreases by F*R.
+* StreamOracle.sink_update -- reading of "sink tokens updated from recent visual context": the
+  sink entries become copies of the last F_s appended frames.
+* noise -- the motion-to-noise-rate map.  PARITY UNPINNED with respect to the pages: they give
+  no formula and disagree on its direction (gist summary 2.A.3 vs review page section 三); the
+  map is a declared reading, pinned only to its own stated properties (monotone, end points,
+  direction flag, smoothing closed form).
 """
 import ctypes
 import math
@@ -61,6 +70,8 @@ def lib():
         L.orc_ssd_u8.restype = u64
         L.orc_ssd_u8.argtypes = [vp, vp, i64]
         L.orc_motion_ssd.argtypes = [vp, i64, i64, i64, vp]
+        L.orc_noise.argtypes = [vp, i64, i64, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                ctypes.c_float, i32, vp, vp]
         L.orc_num_threads.restype = i32
         L.orc_set_num_threads.argtypes = [i32]
         _LIB = L
@@ -160,7 +171,11 @@ class FrameListCache:
         self.appended = 0          # frames ever appended (distinct frame numbers)
 
     def append(self, frame: int, tpos: int, k, v):
-        for e in self.entries:
+        # A frame that is already retained is replaced where it lives: sink frames (frame < F_s)
+        # in the sink part, later frames in the window part.  (After a sink update the sink
+        # holds copies of window frames; a later denoise step re-appends the window original.)
+        home = self.entries[:self.sink_frames] if frame < self.sink_frames else self.entries[self.sink_frames:]
+        for e in home:
             if e[0] == frame:
                 e[1], e[2], e[3] = tpos, k, v
                 return
@@ -296,6 +311,33 @@ class StreamOracle:
                               np.ascontiguousarray(v_bits[sl]).copy())
         return q_rot
 
+    def refresh_rerotate(self, chunk: int):
+        """At a refresh chunk (R > 0, c > 0, c mod R == 0), before the chunk is appended: every
+        window entry of an earlier chunk has its keys turned back by F*R on the time axis and
+        its time index lowered by F*R.  Returns True if anything changed."""
+        w = self.w
+        R = w.refresh_chunks
+        if not (R > 0 and chunk > 0 and chunk % R == 0):
+            return False
+        shift = w.chunk_frames * R
+        for e in self.cache.entries[w.sink_frames:]:
+            if 0 <= e[0] < chunk * w.chunk_frames:
+                n = e[2].shape[0]
+                z = np.zeros(n, np.int64)
+                e[2] = rope_spec(e[2], np.full(n, -shift, np.int64), z, z, w.rope_t, w.rope_h, w.rope_w,
+                                 w.rope_base)
+                e[1] = e[1] - shift
+        return True
+
+    def sink_update(self):
+        """Replace the sink entries by copies of the last F_s appended frames."""
+        fs = self.w.sink_frames
+        if fs == 0:
+            return
+        last = self.cache.entries[-fs:]
+        assert len(self.cache.entries) >= 2 * fs and all(e[0] >= fs for e in last)
+        self.cache.entries[:fs] = [[e[0], e[1], e[2].copy(), e[3].copy()] for e in last]
+
     def attend(self, q_rot, head: int, rows=None, scale=None):
         """Attention of query rows of q_rot[:, head, :] to every retained key of that head."""
         D = self.w.head_dim
@@ -317,6 +359,20 @@ def motion_ssd(frames: np.ndarray) -> np.ndarray:
     out = np.empty((nb, t1 - 1), np.uint64)
     lib().orc_motion_ssd(_p(f), nb, t1 - 1, npix, _p(out))
     return out
+
+
+def noise(m: np.ndarray, m_lo, m_hi, out_lo, out_hi, ema, more_noise_when_fast, state=None):
+    """Noise rate per frame (see orc_noise).  m: [B][T] float32; state: [B] float32 or None
+    (updated in place).  Returns rate [B][T] float32."""
+    m = np.ascontiguousarray(m, np.float32)
+    B, T = m.shape
+    rate = np.empty_like(m)
+    st = None if state is None else state
+    if st is not None:
+        assert st.dtype == np.float32 and st.flags["C_CONTIGUOUS"]
+    lib().orc_noise(_p(m), B, T, m_lo, m_hi, out_lo, out_hi, ema, int(more_noise_when_fast),
+                    None if st is None else _p(st), _p(rate))
+    return rate
 
 
 def motion_rms(ssd: np.ndarray, npix: int) -> np.ndarray:

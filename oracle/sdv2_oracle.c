@@ -284,6 +284,32 @@ void orc_motion_ssd(const uint8_t* frames, int64_t nb, int64_t T, int64_t npix, 
         }
 }
 
+/* ------------------------------------------------------------------------------------------ */
+/* Motion-aware noise controller (a declared map; the pages give no formula)                    */
+/* ------------------------------------------------------------------------------------------ */
+
+/* rate[b][t] from m[b][t]: u = clamp((m - m_lo)/(m_hi - m_lo), 0, 1), flipped when
+ * more_noise_when_fast == 0; r = fmaf(out_hi - out_lo, u, out_lo); the smoothed value is r for a
+ * stream's first frame (state < 0) and fmaf(ema, s - r, r) afterwards.  fp32, one rounding per
+ * operation as written.  state (nullable) carries s across calls. */
+void orc_noise(const float* m, int64_t nb, int64_t T, float m_lo, float m_hi, float out_lo, float out_hi,
+               float ema, int more_noise_when_fast, float* state, float* rate)
+{
+    for (int64_t b = 0; b < nb; ++b) {
+        float s = state ? state[b] : -1.0f;
+        for (int64_t t = 0; t < T; ++t) {
+            float u = (m[b * T + t] - m_lo) / (m_hi - m_lo);
+            if (u < 0.0f) u = 0.0f;
+            if (u > 1.0f) u = 1.0f;
+            if (!more_noise_when_fast) u = 1.0f - u;
+            const float r = fmaf(out_hi - out_lo, u, out_lo);
+            s = (s < 0.0f) ? r : fmaf(ema, s - r, r);
+            rate[b * T + t] = s;
+        }
+        if (state) state[b] = s;
+    }
+}
+
 int orc_num_threads(void)
 {
 #ifdef _OPENMP

@@ -6,6 +6,7 @@ non-zero status becomes an SDV2Error.  Every step of the path runs in the librar
 there is no fallback -- if the library is missing or cannot be loaded, the calls raise.
 """
 from ._binding import (  # noqa: F401
+    NoiseCtl,
     SDV2Error,
     StreamConfig,
     cache_bytes,
@@ -21,8 +22,11 @@ from ._binding import (  # noqa: F401
     lib_path,
     meta_bytes,
     motion_l2,
+    noise_from_motion,
     rope_append_kv,
+    rope_refresh_rerotate,
     set_wait_timeout_ns,
+    sink_update,
     visible_tokens,
     workspace_bytes,
     workspace_init,

@@ -14,7 +14,8 @@ STATUS_NAMES = {0: "SDV2_OK", 1: "SDV2_ERR_INVALID_ARG", 2: "SDV2_ERR_UNSUPPORTE
 EXPORTS = ["sdv2_workspace_bytes", "sdv2_cache_bytes", "sdv2_meta_bytes", "sdv2_visible_tokens",
            "sdv2_workspace_init", "sdv2_cache_reset", "sdv2_rope_append_kv", "sdv2_chunk_attention",
            "sdv2_chunk_attention_noalloc",
-           "sdv2_motion_l2", "sdv2_check_device_error", "sdv2_set_wait_timeout_ns",
+           "sdv2_motion_l2", "sdv2_rope_refresh_rerotate", "sdv2_sink_update", "sdv2_noise_from_motion",
+           "sdv2_check_device_error", "sdv2_set_wait_timeout_ns",
            "sdv2_debug_drop_kv_tile", "sdv2_debug_set_kv_splits", "sdv2_last_kv_splits",
            "sdv2_status_string", "sdv2_last_error"]
 
@@ -23,6 +24,12 @@ class SDV2Error(RuntimeError):
     def __init__(self, status: int, where: str, detail: str):
         self.status = status
         super().__init__("%s: %s (%s)" % (where, STATUS_NAMES.get(status, str(status)), detail))
+
+
+class NoiseCtl(ctypes.Structure):
+    """Mirror of sdv2_noise_ctl."""
+    _fields_ = [("motion_lo", ctypes.c_float), ("motion_hi", ctypes.c_float), ("rate_lo", ctypes.c_float),
+                ("rate_hi", ctypes.c_float), ("ema", ctypes.c_float), ("more_noise_when_fast", ctypes.c_int32)]
 
 
 class StreamConfig(ctypes.Structure):
@@ -86,6 +93,12 @@ def lib():
         L.sdv2_chunk_attention_noalloc.argtypes = [cfgp, i64p, vp, vp, vp, ctypes.c_float, vp, vp, vp]
         L.sdv2_motion_l2.restype = ctypes.c_int
         L.sdv2_motion_l2.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp, vp]
+        L.sdv2_rope_refresh_rerotate.restype = ctypes.c_int
+        L.sdv2_rope_refresh_rerotate.argtypes = [cfgp, i64p, vp, vp, vp]
+        L.sdv2_sink_update.restype = ctypes.c_int
+        L.sdv2_sink_update.argtypes = [cfgp, i64p, ctypes.POINTER(ctypes.c_int32), vp, vp, vp, vp]
+        L.sdv2_noise_from_motion.restype = ctypes.c_int
+        L.sdv2_noise_from_motion.argtypes = [ctypes.POINTER(NoiseCtl), vp, i32, i64, vp, vp, vp]
         L.sdv2_check_device_error.restype = ctypes.c_int
         L.sdv2_check_device_error.argtypes = [vp, vp]
         L.sdv2_set_wait_timeout_ns.restype = None
@@ -189,6 +202,24 @@ def motion_l2(frames, ssd, m=None, stream=None):
     B, T1, Hp, Wp, C = frames.shape
     _check(lib().sdv2_motion_l2(_ptr(frames), B, T1 - 1, Hp, Wp, C, _ptr(ssd), _ptr(m), _stream(stream)),
            "sdv2_motion_l2")
+
+
+def rope_refresh_rerotate(cfg, chunk_index, k_cache, meta, stream=None):
+    _check(lib().sdv2_rope_refresh_rerotate(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch), _ptr(k_cache),
+                                            _ptr(meta), _stream(stream)), "sdv2_rope_refresh_rerotate")
+
+
+def sink_update(cfg, chunk_index, update, k_cache, v_cache, meta, stream=None):
+    upd = (ctypes.c_int32 * cfg.batch)(*[int(u) for u in update])
+    _check(lib().sdv2_sink_update(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch), upd, _ptr(k_cache),
+                                  _ptr(v_cache), _ptr(meta), _stream(stream)), "sdv2_sink_update")
+
+
+def noise_from_motion(ctl, m, rate, state=None, stream=None):
+    """m, rate: device fp32 [B][T]; state: device fp32 [B] or None."""
+    B, T = m.shape
+    _check(lib().sdv2_noise_from_motion(ctypes.byref(ctl), _ptr(m), B, T, _ptr(state), _ptr(rate), _stream(stream)),
+           "sdv2_noise_from_motion")
 
 
 def check_device_error(ws, stream=None):

@@ -369,6 +369,111 @@ sdv2_status sdv2_motion_l2(const uint8_t* frames, int32_t B, int64_t T, int32_t 
                        "motion_l2 launch");
 }
 
+sdv2_status sdv2_rope_refresh_rerotate(const sdv2_stream_cfg* c, const int64_t* chunk_index, void* k_cache,
+                                       void* meta, void* stream)
+{
+    sdv2_status s = check_cfg(c);
+    if (s != SDV2_OK) return s;
+    if (!chunk_index) return fail(SDV2_ERR_INVALID_ARG, "chunk_index is required");
+    if (!k_cache || !meta || !aligned16(k_cache) || !aligned16(meta))
+        return fail(SDV2_ERR_INVALID_ARG, "k_cache and meta must be non-null and 16-byte aligned");
+    if (c->batch > sdv2::kMaxCacheStreams) return fail(SDV2_ERR_UNSUPPORTED, "more than 64 streams");
+    if (c->rope_t / 2 > sdv2::kMaxTimePairsPerAxis) return fail(SDV2_ERR_UNSUPPORTED, "rope_t > 128");
+    if ((s = check_device()) != SDV2_OK) return s;
+    sdv2::RerotateParams p{};
+    p.k_cache = static_cast<uint16_t*>(k_cache);
+    p.meta = static_cast<sdv2_slot_meta*>(meta);
+    p.B = c->batch;
+    p.H = c->heads;
+    p.HW = static_cast<int32_t>(hw_of(c));
+    p.Fs = c->sink_frames;
+    p.W = c->window_frames;
+    p.nslots = static_cast<int32_t>(slots_of(c));
+    p.tp = c->rope_t / 2;
+    p.tvecs = (p.tp + 3) / 4;
+    const int64_t R = c->refresh_chunks;
+    p.shift = static_cast<int64_t>(c->chunk_frames) * R;
+    bool any = false;
+    for (int b = 0; b < c->batch; ++b) {
+        if (chunk_index[b] < 0) return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be >= 0", b);
+        p.active[b] = (R > 0 && chunk_index[b] > 0 && chunk_index[b] % R == 0) ? 1 : 0;
+        p.limit[b] = chunk_index[b] * c->chunk_frames;
+        any = any || p.active[b];
+    }
+    if (!any || p.tp == 0) return ok();
+    for (int j = 0; j < p.tp; ++j) cos_sin_f32(-p.shift, j, c->rope_t, c->rope_base, &p.cs[j].x);
+    return cuda_status(sdv2::launch_rerotate(p, static_cast<cudaStream_t>(stream)), "rerotate launch");
+}
+
+sdv2_status sdv2_sink_update(const sdv2_stream_cfg* c, const int64_t* chunk_index, const int32_t* update,
+                             void* k_cache, void* v_cache, void* meta, void* stream)
+{
+    sdv2_status s = check_cfg(c);
+    if (s != SDV2_OK) return s;
+    if (!chunk_index || !update) return fail(SDV2_ERR_INVALID_ARG, "chunk_index and update are required");
+    if (!k_cache || !v_cache || !meta || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(meta))
+        return fail(SDV2_ERR_INVALID_ARG, "k_cache, v_cache and meta must be non-null and 16-byte aligned");
+    if (c->batch > sdv2::kMaxCacheStreams) return fail(SDV2_ERR_UNSUPPORTED, "more than 64 streams");
+    if (c->sink_frames > sdv2::kMaxSinkFrames) return fail(SDV2_ERR_UNSUPPORTED, "more than 64 sink frames");
+    if (c->sink_frames == 0) return ok();
+    if (c->window_frames < c->sink_frames)
+        return fail(SDV2_ERR_INVALID_ARG, "a sink update needs window_frames >= sink_frames");
+    sdv2::SinkUpdateParams p{};
+    p.k_cache = static_cast<uint16_t*>(k_cache);
+    p.v_cache = static_cast<uint16_t*>(v_cache);
+    p.meta = static_cast<sdv2_slot_meta*>(meta);
+    p.B = c->batch;
+    p.H = c->heads;
+    p.HW = static_cast<int32_t>(hw_of(c));
+    p.Fs = c->sink_frames;
+    p.nslots = static_cast<int32_t>(slots_of(c));
+    bool any = false;
+    for (int b = 0; b < c->batch; ++b) {
+        if (chunk_index[b] < 0) return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be >= 0", b);
+        p.active[b] = update[b] ? 1 : 0;
+        if (!p.active[b]) continue;
+        const int64_t n = (chunk_index[b] + 1) * c->chunk_frames;   // frames appended so far
+        if (n < 2 * static_cast<int64_t>(c->sink_frames))
+            return fail(SDV2_ERR_INVALID_ARG, "stream %d: a sink update needs at least 2*sink_frames frames", b);
+        for (int i = 0; i < c->sink_frames; ++i)
+            p.src_slot[b * sdv2::kMaxSinkFrames + i] = static_cast<int32_t>(slot_of(c, n - c->sink_frames + i));
+        any = true;
+    }
+    if (!any) return ok();
+    if ((s = check_device()) != SDV2_OK) return s;
+    return cuda_status(sdv2::launch_sink_update(p, static_cast<cudaStream_t>(stream)), "sink update launch");
+}
+
+sdv2_status sdv2_noise_from_motion(const sdv2_noise_ctl* ctl, const float* m, int32_t B, int64_t T, float* state,
+                                   float* rate, void* stream)
+{
+    if (!ctl || !m || !rate) return fail(SDV2_ERR_INVALID_ARG, "ctl, m and rate are required");
+    if (B < 1 || T < 1) return fail(SDV2_ERR_INVALID_ARG, "B and T must be >= 1");
+    if (!(ctl->motion_hi > ctl->motion_lo) || !std::isfinite(ctl->motion_lo) || !std::isfinite(ctl->motion_hi))
+        return fail(SDV2_ERR_INVALID_ARG, "motion_hi must be > motion_lo (both finite)");
+    if (!(ctl->rate_lo >= 0.f) || !(ctl->rate_hi >= 0.f) || !std::isfinite(ctl->rate_lo) || !std::isfinite(ctl->rate_hi))
+        return fail(SDV2_ERR_INVALID_ARG, "rates must be finite and >= 0");
+    if (!(ctl->ema >= 0.f && ctl->ema < 1.f)) return fail(SDV2_ERR_INVALID_ARG, "ema must be in [0, 1)");
+    const void* ptrs[] = {m, rate};
+    for (const void* p : ptrs)
+        if ((reinterpret_cast<uintptr_t>(p) & 3u)) return fail(SDV2_ERR_INVALID_ARG, "m and rate must be 4-byte aligned");
+    sdv2_status s = check_device();
+    if (s != SDV2_OK) return s;
+    sdv2::NoiseParams p{};
+    p.m = m;
+    p.rate = rate;
+    p.state = state;
+    p.B = B;
+    p.T = T;
+    p.m_lo = ctl->motion_lo;
+    p.m_hi = ctl->motion_hi;
+    p.out_lo = ctl->rate_lo;
+    p.out_hi = ctl->rate_hi;
+    p.ema = ctl->ema;
+    p.more_noise_when_fast = ctl->more_noise_when_fast;
+    return cuda_status(sdv2::launch_noise(p, static_cast<cudaStream_t>(stream)), "noise controller launch");
+}
+
 sdv2_status sdv2_check_device_error(void* ws, void* stream)
 {
     if (!ws) return fail(SDV2_ERR_INVALID_ARG, "ws is NULL");

@@ -96,6 +96,47 @@ int choose_kv_splits(int64_t items, int min_tiles, int slots);
 cudaError_t launch_motion_l2(const uint8_t* frames, int B, int64_t T, int64_t frame_bytes,
                              uint64_t* ssd, float* m, cudaStream_t s);
 
+// ---- refresh re-rotation, sink update, noise controller ------------------------------------
+
+constexpr int kMaxTimePairsPerAxis = 64;
+constexpr int kMaxSinkFrames = 64;
+constexpr int kMaxCacheStreams = 64;
+
+struct RerotateParams {
+    uint16_t* k_cache;
+    sdv2_slot_meta* meta;
+    int32_t B, H, HW, Fs, W, nslots;
+    int32_t tp;                              // time-axis rotation pairs
+    int32_t tvecs;                           // 16-byte vectors that hold time-axis dims
+    int64_t shift;                           // F*R: subtracted from the slots' tpos
+    int32_t active[kMaxCacheStreams];        // stream is at a refresh chunk
+    int64_t limit[kMaxCacheStreams];         // frames below c*F are re-rotated
+    float2 cs[kMaxTimePairsPerAxis];         // (cos, sin) of the angle -F*R*omega_j
+};
+
+struct SinkUpdateParams {
+    uint16_t* k_cache;
+    uint16_t* v_cache;
+    sdv2_slot_meta* meta;
+    int32_t B, H, HW, Fs, nslots;
+    int32_t active[kMaxCacheStreams];
+    int32_t src_slot[kMaxCacheStreams * kMaxSinkFrames];   // [b][s]: window slot copied into sink slot s
+};
+
+struct NoiseParams {
+    const float* m;
+    float* rate;
+    float* state;                            // [B] or null
+    int32_t B;
+    int64_t T;
+    float m_lo, m_hi, out_lo, out_hi, ema;
+    int32_t more_noise_when_fast;
+};
+
+cudaError_t launch_rerotate(const RerotateParams& p, cudaStream_t s);
+cudaError_t launch_sink_update(const SinkUpdateParams& p, cudaStream_t s);
+cudaError_t launch_noise(const NoiseParams& p, cudaStream_t s);
+
 // Sets the per-thread message returned by sdv2_last_error().
 void set_last_error(const char* msg);
 

@@ -91,6 +91,29 @@ class LockStep:
                         assert not kc[b][:, s * hw:(s + 1) * hw, :].any()
                         assert not vc[b][:, s * hw:(s + 1) * hw, :].any()
 
+    def check_cache_entries_in_slots(self):
+        """Sink entries live in slots 0..F_s-1 in list order (after a sink update they are
+        copies of window frames); window entries live in their ring slots.  Bit-exact rows
+        and metadata, and nothing else is filled."""
+        w = self.w
+        L = self.sess.layers[0]
+        kc, vc = bits(L.k), bits(L.v)
+        meta = L.meta.cpu().numpy()
+        hw = w.hw
+        for b in range(w.batch):
+            entries = self.oracles[b].cache.entries
+            filled = set()
+            for idx, (frame, tpos, kf, vf) in enumerate(entries):
+                s = idx if idx < w.sink_frames else oracle.slot_of_frame(frame, w.sink_frames, w.window_frames)
+                assert s not in filled
+                filled.add(s)
+                assert tuple(meta[b, s]) == (frame, tpos), (b, s, tuple(meta[b, s]), frame, tpos)
+                np.testing.assert_array_equal(kc[b][:, s * hw:(s + 1) * hw, :], kf.transpose(1, 0, 2),
+                                              err_msg="k slot %d stream %d" % (s, b))
+                np.testing.assert_array_equal(vc[b][:, s * hw:(s + 1) * hw, :], vf.transpose(1, 0, 2),
+                                              err_msg="v slot %d stream %d" % (s, b))
+            assert filled == set(range(len(filled)))
+
     def check_attention(self, q_rot_o, rows=None, heads=None, check_lse=True):
         w = self.w
         out = to_f64(self.sess.out)                     # [B][Nq][H][D]
