@@ -147,6 +147,30 @@ sdv2_status sdv2_rope_append_kv(const sdv2_stream_cfg* cfg, const int64_t* start
                                 void* meta, void* ws, void* stream);
 
 /*
+ * Fused QKV projection + Causal-RoPE + cache append ("Accelerating Video Generation Inference
+ * with Sequential-Parallel 3D Positional Encoding Using a Global Time Index", technical summary
+ * 2(다): the QKV projection and the Causal-RoPE computation fused into one kernel).
+ *
+ * For every token of chunk chunk_index[b] of every stream b:
+ *   [q | k | v] = W_qkv x + bias   (features: q head h dim d at h*D + d, then k, then v)
+ * then q and k are rotated with the token's 3D RoPE (positions exactly as sdv2_rope_append_kv)
+ * and q_rot, the cache rows of the chunk's frames and their slot metadata are written as by
+ * sdv2_rope_append_kv.
+ * x: device bf16 [B][Nq][C] with C = H*D, tokens x_token_stride elements apart (0 = C;
+ *   a multiple of 8); streams Nq*x_token_stride apart.
+ * w_qkv: device bf16 [3*H*D][C] (row = output feature); bias: device fp32 [3*H*D] or NULL.
+ * q_rot, k_cache, v_cache, meta, ws: as sdv2_rope_append_kv.
+ * Numerics: bf16 products with fp32 accumulation (tcgen05 tensor cores), + bias in fp32, q/k
+ * pairs rotated in fp32 as (fmaf(x, c, -(y*s)), fmaf(x, s, y*c)), one bf16 RNE per output.
+ * (It differs from projecting to bf16 first and calling sdv2_rope_append_kv by that one
+ * rounding.)  Limits: H even; the limits of sdv2_rope_append_kv.
+ */
+sdv2_status sdv2_qkv_rope_append(const sdv2_stream_cfg* cfg, const int64_t* start_frame,
+                                 const int64_t* chunk_index, const void* x, int64_t x_token_stride,
+                                 const void* w_qkv, const float* bias, void* q_rot, void* k_cache,
+                                 void* v_cache, void* meta, void* ws, void* stream);
+
+/*
  * Chunk attention: out[b][n][h][:] = sum_j softmax_j(scale * <q_rot[b][h][n], k_j>) v_j over
  * the valid cache rows j < sdv2_visible_tokens(cfg, chunk_index[b]) of stream b, head h.
  * There is no mask inside the valid rows: the chunk attends to itself in full and to every

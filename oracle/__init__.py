@@ -25,6 +25,9 @@ What each function follows (pages are cited by title and section):
   (-F*R, 0, 0)), and their time index decreases by F*R.
 * StreamOracle.sink_update -- reading of "sink tokens updated from recent visual context": the
   sink entries become copies of the last F_s appended frames.
+* qkv_project -- the QKV projection W x + bias in fp64 (numpy's matmul as the product
+  primitive), for the fused projection + Causal-RoPE path of the Causal-RoPE page, technical
+  summary 2(다); its output is rotated with rope_ideal.
 * noise -- the motion-to-noise-rate map.  PARITY UNPINNED with respect to the pages: they give
   no formula and disagree on its direction (gist summary 2.A.3 vs review page section 三); the
   map is a declared reading, pinned only to its own stated properties (monotone, end points,
@@ -359,6 +362,16 @@ def motion_ssd(frames: np.ndarray) -> np.ndarray:
     out = np.empty((nb, t1 - 1), np.uint64)
     lib().orc_motion_ssd(_p(f), nb, t1 - 1, npix, _p(out))
     return out
+
+
+def qkv_project(x_bits: np.ndarray, w_bits: np.ndarray, bias=None) -> np.ndarray:
+    """fp64 [M][N] = x [M][C] (bf16 bits) times w [N][C]^T (bf16 bits) plus bias [N] (fp32)."""
+    x = bf16_to_f32(x_bits).astype(np.float64)
+    w = bf16_to_f32(w_bits).astype(np.float64)
+    y = x @ w.T
+    if bias is not None:
+        y = y + np.asarray(bias, np.float32).astype(np.float64)[None, :]
+    return y
 
 
 def noise(m: np.ndarray, m_lo, m_hi, out_lo, out_hi, ema, more_noise_when_fast, state=None):

@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     meta_bytes,
     motion_l2,
     noise_from_motion,
+    qkv_rope_append,
     rope_append_kv,
     rope_refresh_rerotate,
     set_wait_timeout_ns,

@@ -12,7 +12,7 @@ STATUS_NAMES = {0: "SDV2_OK", 1: "SDV2_ERR_INVALID_ARG", 2: "SDV2_ERR_UNSUPPORTE
 
 # Every symbol that include/sdv2.h declares.
 EXPORTS = ["sdv2_workspace_bytes", "sdv2_cache_bytes", "sdv2_meta_bytes", "sdv2_visible_tokens",
-           "sdv2_workspace_init", "sdv2_cache_reset", "sdv2_rope_append_kv", "sdv2_chunk_attention",
+           "sdv2_workspace_init", "sdv2_cache_reset", "sdv2_rope_append_kv", "sdv2_qkv_rope_append", "sdv2_chunk_attention",
            "sdv2_chunk_attention_noalloc",
            "sdv2_motion_l2", "sdv2_rope_refresh_rerotate", "sdv2_sink_update", "sdv2_noise_from_motion",
            "sdv2_check_device_error", "sdv2_set_wait_timeout_ns",
@@ -87,6 +87,8 @@ def lib():
         L.sdv2_cache_reset.argtypes = [cfgp, vp, vp, vp, vp]
         L.sdv2_rope_append_kv.restype = ctypes.c_int
         L.sdv2_rope_append_kv.argtypes = [cfgp, i64p, i64p, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.sdv2_qkv_rope_append.restype = ctypes.c_int
+        L.sdv2_qkv_rope_append.argtypes = [cfgp, i64p, i64p, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
         L.sdv2_chunk_attention.restype = ctypes.c_int
         L.sdv2_chunk_attention.argtypes = [cfgp, i64p, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
         L.sdv2_chunk_attention_noalloc.restype = ctypes.c_int
@@ -182,6 +184,16 @@ def rope_append_kv(cfg, start_frame, chunk_index, q, k, v, q_rot, k_cache, v_cac
     _check(lib().sdv2_rope_append_kv(ctypes.byref(cfg), _i64_array(start_frame, B), _i64_array(chunk_index, B),
                                      _ptr(q), _ptr(k), _ptr(v), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache),
                                      _ptr(meta), _ptr(ws), _stream(stream)), "sdv2_rope_append_kv")
+
+
+def qkv_rope_append(cfg, start_frame, chunk_index, x, w_qkv, q_rot, k_cache, v_cache, meta, ws, bias=None,
+                    x_token_stride=0, stream=None):
+    """x: [B][Nq][H*D] bf16; w_qkv: [3*H*D][H*D] bf16; bias: fp32 [3*H*D] or None."""
+    B = cfg.batch
+    _check(lib().sdv2_qkv_rope_append(ctypes.byref(cfg), _i64_array(start_frame, B), _i64_array(chunk_index, B),
+                                      _ptr(x), int(x_token_stride), _ptr(w_qkv), _ptr(bias), _ptr(q_rot),
+                                      _ptr(k_cache), _ptr(v_cache), _ptr(meta), _ptr(ws), _stream(stream)),
+           "sdv2_qkv_rope_append")
 
 
 def chunk_attention(cfg, chunk_index, q_rot, k_cache, v_cache, out, ws, lse=None, scale=0.0, stream=None):

@@ -91,22 +91,41 @@ __global__ void sink_update_kernel(const __grid_constant__ SinkUpdateParams p)
         p.meta[static_cast<int64_t>(b) * p.nslots + s] = p.meta[static_cast<int64_t>(b) * p.nslots + src];
 }
 
-// One thread per stream walks its T motion values in order (the smoothing is sequential).
-__global__ void noise_kernel(const __grid_constant__ NoiseParams p)
+// One block per stream: the block stages up to kNoiseTile motion values in shared memory, one
+// thread walks them in order (the smoothing is a sequential recurrence, kept in the oracle's
+// order and rounding), and the block writes the rates back.
+constexpr int kNoiseThreads = 256;
+constexpr int kNoiseTile = 4096;
+
+__global__ void __launch_bounds__(kNoiseThreads) noise_kernel(const __grid_constant__ NoiseParams p)
 {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= p.B) return;
-    float state = p.state ? p.state[b] : -1.0f;
-    for (int64_t t = 0; t < p.T; ++t) {
-        const float m = p.m[static_cast<int64_t>(b) * p.T + t];
-        float u = (m - p.m_lo) / (p.m_hi - p.m_lo);
-        u = fminf(fmaxf(u, 0.0f), 1.0f);
-        if (!p.more_noise_when_fast) u = 1.0f - u;
-        const float r = __fmaf_rn(p.out_hi - p.out_lo, u, p.out_lo);
-        state = (state < 0.0f) ? r : __fmaf_rn(p.ema, state - r, r);   // ema*state + (1-ema)*r
-        p.rate[static_cast<int64_t>(b) * p.T + t] = state;
+    __shared__ float buf[kNoiseTile];
+    __shared__ float carry;
+    const int b = blockIdx.x;
+    if (threadIdx.x == 0) carry = p.state ? p.state[b] : -1.0f;
+    const float* m = p.m + static_cast<int64_t>(b) * p.T;
+    float* rate = p.rate + static_cast<int64_t>(b) * p.T;
+    for (int64_t t0 = 0; t0 < p.T; t0 += kNoiseTile) {
+        const int n = static_cast<int>((p.T - t0 < kNoiseTile) ? (p.T - t0) : kNoiseTile);
+        for (int i = threadIdx.x; i < n; i += kNoiseThreads) buf[i] = m[t0 + i];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float state = carry;
+            for (int i = 0; i < n; ++i) {
+                float u = (buf[i] - p.m_lo) / (p.m_hi - p.m_lo);
+                u = fminf(fmaxf(u, 0.0f), 1.0f);
+                if (!p.more_noise_when_fast) u = 1.0f - u;
+                const float r = __fmaf_rn(p.out_hi - p.out_lo, u, p.out_lo);
+                state = (state < 0.0f) ? r : __fmaf_rn(p.ema, state - r, r);   // ema*state + (1-ema)*r
+                buf[i] = state;
+            }
+            carry = state;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += kNoiseThreads) rate[t0 + i] = buf[i];
+        __syncthreads();
     }
-    if (p.state) p.state[b] = state;
+    if (threadIdx.x == 0 && p.state) p.state[b] = carry;
 }
 
 }  // namespace
@@ -129,7 +148,7 @@ cudaError_t launch_sink_update(const SinkUpdateParams& p, cudaStream_t s)
 
 cudaError_t launch_noise(const NoiseParams& p, cudaStream_t s)
 {
-    noise_kernel<<<(p.B + 127) / 128, 128, 0, s>>>(p);
+    noise_kernel<<<p.B, kNoiseThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -110,6 +110,42 @@ void cos_sin_f32(int64_t pos, int j, int d, double base, float* cs)
     cs[1] = static_cast<float>(std::sin(th));
 }
 
+// Frame descriptors (slot, stream-relative frame, time index) and the time-axis (cos, sin)
+// rows of one chunk of every stream: entries b*F + i.
+void fill_frames(const sdv2_stream_cfg* c, const int64_t* start_frame, const int64_t* chunk_index,
+                 sdv2::FrameDesc* frames, float2* tcs)
+{
+    const int F = c->chunk_frames, tp = c->rope_t / 2;
+    for (int b = 0; b < c->batch; ++b) {
+        const int64_t cidx = chunk_index[b];
+        const int64_t ceff = c->refresh_chunks > 0 ? cidx % c->refresh_chunks : cidx;
+        for (int i = 0; i < F; ++i) {
+            sdv2::FrameDesc& fd = frames[b * F + i];
+            fd.frame = cidx * F + i;
+            fd.tpos = start_frame[b] + ceff * F + i;
+            fd.slot = static_cast<int32_t>(slot_of(c, fd.frame));
+            for (int j = 0; j < tp; ++j) cos_sin_f32(fd.tpos, j, c->rope_t, c->rope_base, &tcs[(b * F + i) * tp + j].x);
+        }
+    }
+}
+
+// Checks shared by the two append entry points: host arrays, sizes of the per-call tables.
+sdv2_status check_append_args(const sdv2_stream_cfg* c, const int64_t* start_frame, const int64_t* chunk_index)
+{
+    if (!start_frame || !chunk_index) return fail(SDV2_ERR_INVALID_ARG, "start_frame and chunk_index are required");
+    const int B = c->batch, F = c->chunk_frames, tp = c->rope_t / 2;
+    if (static_cast<int64_t>(B) * F > sdv2::kMaxChunkFrames || static_cast<int64_t>(B) * F * tp > sdv2::kMaxTimePairs)
+        return fail(SDV2_ERR_UNSUPPORTED, "B*F (%d) must be <= %d and B*F*rope_t/2 (%d) <= %d", B * F,
+                    sdv2::kMaxChunkFrames, B * F * tp, sdv2::kMaxTimePairs);
+    for (int b = 0; b < B; ++b) {
+        if (start_frame[b] < 0 || chunk_index[b] < 0)
+            return fail(SDV2_ERR_INVALID_ARG, "start_frame[%d] and chunk_index[%d] must be >= 0", b, b);
+        if (chunk_index[b] > (int64_t(1) << 40) || start_frame[b] > (int64_t(1) << 50))
+            return fail(SDV2_ERR_INVALID_ARG, "start_frame[%d] or chunk_index[%d] too large", b, b);
+    }
+    return SDV2_OK;
+}
+
 // sm_103 check, cached per device.
 sdv2_status check_device()
 {
@@ -262,20 +298,11 @@ sdv2_status sdv2_rope_append_kv(const sdv2_stream_cfg* c, const int64_t* start_f
 {
     sdv2_status s = check_cfg(c);
     if (s != SDV2_OK) return s;
-    if (!start_frame || !chunk_index) return fail(SDV2_ERR_INVALID_ARG, "start_frame and chunk_index are required");
     const void* ptrs[] = {q, k, v, q_rot, k_cache, v_cache, meta, ws};
     for (const void* p : ptrs)
         if (!p || !aligned16(p)) return fail(SDV2_ERR_INVALID_ARG, "device pointers must be non-null and 16-byte aligned");
+    if ((s = check_append_args(c, start_frame, chunk_index)) != SDV2_OK) return s;
     const int B = c->batch, F = c->chunk_frames, tp = c->rope_t / 2;
-    if (static_cast<int64_t>(B) * F > sdv2::kMaxChunkFrames || static_cast<int64_t>(B) * F * tp > sdv2::kMaxTimePairs)
-        return fail(SDV2_ERR_UNSUPPORTED, "B*F (%d) must be <= %d and B*F*rope_t/2 (%d) <= %d", B * F,
-                    sdv2::kMaxChunkFrames, B * F * tp, sdv2::kMaxTimePairs);
-    for (int b = 0; b < B; ++b) {
-        if (start_frame[b] < 0 || chunk_index[b] < 0)
-            return fail(SDV2_ERR_INVALID_ARG, "start_frame[%d] and chunk_index[%d] must be >= 0", b, b);
-        if (chunk_index[b] > (int64_t(1) << 40) || start_frame[b] > (int64_t(1) << 50))
-            return fail(SDV2_ERR_INVALID_ARG, "start_frame[%d] or chunk_index[%d] too large", b, b);
-    }
     if ((s = check_device()) != SDV2_OK) return s;
 
     static thread_local sdv2::RopeAppendParams p;
@@ -302,17 +329,7 @@ sdv2_status sdv2_rope_append_kv(const sdv2_stream_cfg* c, const int64_t* start_f
     p.tp = tp;
     p.hp = c->rope_h / 2;
     p.wp = c->rope_w / 2;
-    for (int b = 0; b < B; ++b) {
-        const int64_t cidx = chunk_index[b];
-        const int64_t ceff = c->refresh_chunks > 0 ? cidx % c->refresh_chunks : cidx;
-        for (int i = 0; i < F; ++i) {
-            sdv2::FrameDesc& fd = p.frames[b * F + i];
-            fd.frame = cidx * F + i;
-            fd.tpos = start_frame[b] + ceff * F + i;
-            fd.slot = static_cast<int32_t>(slot_of(c, fd.frame));
-            for (int j = 0; j < tp; ++j) cos_sin_f32(fd.tpos, j, c->rope_t, c->rope_base, &p.tcs[(b * F + i) * tp + j].x);
-        }
-    }
+    fill_frames(c, start_frame, chunk_index, p.frames, p.tcs);
     return cuda_status(sdv2::launch_rope_append(p, static_cast<cudaStream_t>(stream)), "rope_append launch");
 }
 
@@ -367,6 +384,54 @@ sdv2_status sdv2_motion_l2(const uint8_t* frames, int32_t B, int64_t T, int32_t 
     if (s != SDV2_OK) return s;
     return cuda_status(sdv2::launch_motion_l2(frames, B, T, npix, ssd, m, static_cast<cudaStream_t>(stream)),
                        "motion_l2 launch");
+}
+
+sdv2_status sdv2_qkv_rope_append(const sdv2_stream_cfg* c, const int64_t* start_frame, const int64_t* chunk_index,
+                                  const void* x, int64_t x_token_stride, const void* w_qkv, const float* bias,
+                                  void* q_rot, void* k_cache, void* v_cache, void* meta, void* ws, void* stream)
+{
+    sdv2_status s = check_cfg(c);
+    if (s != SDV2_OK) return s;
+    if ((s = check_append_args(c, start_frame, chunk_index)) != SDV2_OK) return s;
+    const void* ptrs[] = {x, w_qkv, q_rot, k_cache, v_cache, meta, ws};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return fail(SDV2_ERR_INVALID_ARG, "device pointers must be non-null and 16-byte aligned");
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 15u)) return fail(SDV2_ERR_INVALID_ARG, "bias must be 16-byte aligned");
+    const int64_t C = static_cast<int64_t>(c->heads) * c->head_dim;
+    if (c->heads % 2) return fail(SDV2_ERR_UNSUPPORTED, "the fused projection needs an even number of heads");
+    const int64_t ld = x_token_stride ? x_token_stride : C;
+    if (ld < C || (ld % 8)) return fail(SDV2_ERR_INVALID_ARG, "x_token_stride must be >= H*D and a multiple of 8");
+    const int64_t M = static_cast<int64_t>(c->batch) * hw_of(c) * c->chunk_frames;
+    if (M > (int64_t(1) << 31) - 256) return fail(SDV2_ERR_UNSUPPORTED, "too many tokens");
+    if ((s = check_device()) != SDV2_OK) return s;
+    static thread_local sdv2::QkvRopeParams p;
+    std::memset(&p, 0, sizeof(p));
+    const WsLayout L = ws_layout(c);
+    p.bias = bias;
+    p.q_rot = static_cast<uint16_t*>(q_rot);
+    p.k_cache = static_cast<uint16_t*>(k_cache);
+    p.v_cache = static_cast<uint16_t*>(v_cache);
+    p.meta = static_cast<sdv2_slot_meta*>(meta);
+    p.h_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + L.htab);
+    p.w_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + L.wtab);
+    p.err = static_cast<uint32_t*>(ws);
+    p.timeout_ns = g_timeout_ns.load();
+    p.M = static_cast<int32_t>(M);
+    p.C = static_cast<int32_t>(C);
+    p.B = c->batch;
+    p.H = c->heads;
+    p.HW = static_cast<int32_t>(hw_of(c));
+    p.grid_w = c->grid_w;
+    p.F = c->chunk_frames;
+    p.nslots = static_cast<int32_t>(slots_of(c));
+    p.Nq = static_cast<int32_t>(hw_of(c) * c->chunk_frames);
+    p.tp = c->rope_t / 2;
+    p.hp = c->rope_h / 2;
+    p.wp = c->rope_w / 2;
+    fill_frames(c, start_frame, chunk_index, p.frames, p.tcs);
+    const char* why = "launch";
+    cudaError_t e = sdv2::launch_qkv_rope(p, x, w_qkv, ld, static_cast<cudaStream_t>(stream), &why);
+    return cuda_status(e, why);
 }
 
 sdv2_status sdv2_rope_refresh_rerotate(const sdv2_stream_cfg* c, const int64_t* chunk_index, void* k_cache,

@@ -137,6 +137,30 @@ cudaError_t launch_rerotate(const RerotateParams& p, cudaStream_t s);
 cudaError_t launch_sink_update(const SinkUpdateParams& p, cudaStream_t s);
 cudaError_t launch_noise(const NoiseParams& p, cudaStream_t s);
 
+// ---- fused QKV projection + Causal-RoPE + cache append -------------------------------------
+
+struct QkvRopeParams {
+    CUtensorMap xmap;                         // x: [M = B*Nq][C] bf16
+    CUtensorMap wmap;                         // w_qkv: [3*H*D][C] bf16
+    const float* bias;                        // [3*H*D] or null
+    uint16_t* q_rot;
+    uint16_t* k_cache;
+    uint16_t* v_cache;
+    sdv2_slot_meta* meta;
+    const float2* h_tab;
+    const float2* w_tab;
+    uint32_t* err;
+    uint64_t timeout_ns;
+    int32_t M, C, B, H, HW, grid_w, F, nslots, Nq;
+    int32_t tp, hp, wp;
+    FrameDesc frames[kMaxChunkFrames];
+    float2 tcs[kMaxTimePairs];
+};
+
+// Encodes the tensor maps (x rows `x_ld` elements apart) and launches.
+cudaError_t launch_qkv_rope(QkvRopeParams& p, const void* x, const void* w, int64_t x_ld, cudaStream_t s,
+                            const char** why);
+
 // Sets the per-thread message returned by sdv2_last_error().
 void set_last_error(const char* msg);
 

@@ -1,0 +1,285 @@
+// Fused QKV projection + Causal-RoPE + KV-cache append.
+//
+// "Accelerating Video Generation Inference with Sequential-Parallel 3D Positional Encoding
+// Using a Global Time Index", technical summary 2(다): the QKV projection and the Causal-RoPE
+// computation are fused into a single kernel (there in TileLang on A800), with the cos/sin
+// frequencies precomputed into contiguous tables.  Here: one tcgen05 GEMM
+//     [q | k | v][token] = W_qkv x[token] (+ bias),   W_qkv: [3*H*D][C],  x: [B*Nq][C]
+// whose epilogue rotates q and k with the token's 3D RoPE (time index from the stream's start
+// frame and chunk, as in sdv2_rope_append_kv) and writes q_rot (head-major) and k_rot, v into
+// the frames' cache slots, without a round trip of q, k, v through memory.
+//
+// Tiling: a CTA computes 128 tokens x 256 features (two heads of one of q, k, v) over the whole
+// hidden dimension in steps of 64 (128-byte swizzled TMA boxes), through a 2-stage ring
+// (48 KB per stage), so that two CTAs share an SM and one's epilogue overlaps the other's main
+// loop.  The accumulator (128 lanes x 256 fp32 columns) lives in tensor memory.
+//   warp 0: TMA producer; warp 1: MMA issuer (converged, elect.sync); warps 2-5: epilogue,
+//   thread = token row = TMEM lane.
+// Rounding: acc (fp32, fp32 accumulation) + bias (fp32 add); q and k pairs rotated in fp32 as
+// (fmaf(x, c, -(y*s)), fmaf(x, s, y*c)); one bf16 round-to-nearest-even per output.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sdv2 {
+namespace {
+
+constexpr int QBM = 128;                       // tokens per tile
+constexpr int QBN = 256;                       // features per tile
+constexpr int QBK = 64;                        // hidden elements per step (128 bytes of bf16)
+constexpr int QST = 2;                         // ring stages
+constexpr uint32_t A_BYTES = QBM * QBK * 2;    // 16 KB
+constexpr uint32_t B_BYTES = QBN * QBK * 2;    // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int QTHREADS = 6 * 32;
+constexpr uint32_t QTMEM_COLS = 256;
+constexpr uint32_t QSMEM_BYTES = QST * STAGE_BYTES + 256 + 1024;
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constant__ QkvRopeParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s0 = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QST * STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    // barriers: full[QST], empty[QST], acc_full
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * QST + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+#define QBAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
+    const int lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * QBM;
+    const int n0 = blockIdx.y * QBN;
+    const int ksteps = p.C / QBK;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < QST; ++i) {
+            mbar_init(QBAR(i), 1);
+            mbar_init(QBAR(QST + i), 1);
+        }
+        mbar_init(QBAR(2 * QST), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), QTMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.xmap);
+            tma_prefetch_desc(&p.wmap);
+            int pend[QST] = {};
+            uint32_t par[QST] = {};
+            for (int kk = 0; kk < ksteps; ++kk) {
+                const int st = kk % QST;
+                const uint32_t ph = static_cast<uint32_t>(kk / QST) & 1u;
+                if (!mbar_wait_bounded(QBAR(QST + st), ph ^ 1u, tmo, abort_flag)) {
+                    *abort_flag = 1;
+                    atomicOr(p.err, kErrTimeout);
+                    break;
+                }
+                const uint32_t sa = s0 + st * STAGE_BYTES;
+                mbar_arrive_expect_tx(QBAR(st), STAGE_BYTES);
+                tma_load_3d(sa, &p.xmap, QBAR(st), kk * QBK, m0, 0);
+                tma_load_3d(sa + A_BYTES, &p.wmap, QBAR(st), kk * QBK, n0, 0);
+                pend[st] = 1;
+                par[st] = ph;
+            }
+            volatile int no_abort = 0;
+            for (int i = 0; i < QST; ++i)
+                if (pend[i]) mbar_wait_bounded(QBAR(i), par[i], tmo, &no_abort);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32(QBM, QBN, false);
+        const uint64_t dA = sdesc_sw128(s0, 16, 1024);
+        const uint64_t dB = sdesc_sw128(s0 + A_BYTES, 16, 1024);
+        constexpr uint64_t kStage = STAGE_BYTES >> 4;
+        bool ok = true;
+        for (int kk = 0; kk < ksteps; ++kk) {
+            const int st = kk % QST;
+            int r = 1;
+            if (lane == 0) r = mbar_wait_bounded(QBAR(st), static_cast<uint32_t>(kk / QST) & 1u, tmo, abort_flag) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, r, 0)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t a = dA + static_cast<uint64_t>(st) * kStage;
+            const uint64_t b = dB + static_cast<uint64_t>(st) * kStage;
+#pragma unroll
+            for (int k = 0; k < QBK / 16; ++k)
+                mma_ss_warp(tmem, a + static_cast<uint64_t>(k * 2), b + static_cast<uint64_t>(k * 2), idesc,
+                            (kk > 0 || k > 0) ? 1u : 0u);
+            mma_commit_warp(QBAR(QST + st));
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(p.err, kErrTimeout);
+        }
+        mma_commit_warp(QBAR(2 * QST));   // accumulator complete (or drained after an abort)
+        // Tensor memory is freed only after every MMA of this warp has completed.
+        if (lane == 0) {
+            volatile int no_abort = 0;
+            mbar_wait_bounded(QBAR(2 * QST), 0, tmo, &no_abort);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue: 128 threads
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        bool ok = mbar_wait_bounded(QBAR(2 * QST), 0, tmo, abort_flag) && !*abort_flag;
+        if (!ok && row == 0) atomicOr(p.err, kErrTimeout);
+        tc_fence_after();
+        const int m = m0 + row;
+        const bool valid = ok && m < p.M;
+        const int mm = valid ? m : 0;
+        const int b = mm / p.Nq;
+        const int n = mm - b * p.Nq;
+        const int i = n / p.HW;
+        const int r = n - i * p.HW;
+        const int gh = r / p.grid_w;
+        const int gw = r - gh * p.grid_w;
+        const FrameDesc fd = p.frames[b * p.F + i];
+        const int hd = p.H * 128;
+        const int type = n0 / hd;                      // 0 = q, 1 = k, 2 = v
+        const int head0 = (n0 - type * hd) / 128;
+        const int64_t rows = static_cast<int64_t>(p.nslots) * p.HW;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+            const int head = head0 + hh;
+            const int64_t bh = static_cast<int64_t>(b) * p.H + head;
+            uint16_t* dst = (type == 0) ? p.q_rot + (bh * p.Nq + n) * 128
+                          : (type == 1) ? p.k_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128
+                                        : p.v_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128;
+#pragma unroll 1
+            for (int cchunk = 0; cchunk < 4; ++cchunk) {
+                uint32_t a[32];
+                tmem_ld_x32_sync(trow + static_cast<uint32_t>(hh * 128 + cchunk * 32), a);
+                if (!valid) continue;
+                const int f0 = n0 + hh * 128 + cchunk * 32;   // feature of a[0]
+                uint32_t o[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    float x = __uint_as_float(a[2 * u]);
+                    float y = __uint_as_float(a[2 * u + 1]);
+                    if (p.bias) {
+                        x = __fadd_rn(x, p.bias[f0 + 2 * u]);
+                        y = __fadd_rn(y, p.bias[f0 + 2 * u + 1]);
+                    }
+                    if (type < 2) {
+                        const int pr = cchunk * 16 + u;       // rotation pair inside the head
+                        float2 cs;
+                        if (pr < p.tp) cs = p.tcs[(b * p.F + i) * p.tp + pr];
+                        else if (pr < p.tp + p.hp) cs = p.h_tab[gh * p.hp + (pr - p.tp)];
+                        else cs = p.w_tab[gw * p.wp + (pr - p.tp - p.hp)];
+                        const float xr = __fmaf_rn(x, cs.x, -__fmul_rn(y, cs.y));
+                        const float yr = __fmaf_rn(x, cs.y, __fmul_rn(y, cs.x));
+                        x = xr;
+                        y = yr;
+                    }
+                    o[u] = pack2(x, y);
+                }
+                uint4* d4 = reinterpret_cast<uint4*>(dst + cchunk * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            }
+        }
+        if (valid && type == 1 && head0 == 0 && r == 0) {
+            sdv2_slot_meta md;
+            md.frame_id = fd.frame;
+            md.tpos = fd.tpos;
+            p.meta[static_cast<int64_t>(b) * p.nslots + fd.slot] = md;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, QTMEM_COLS);
+    }
+#undef QBAR
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::atomic<int> tried{0};
+    if (!tried.exchange(1)) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// [rows][cols] bf16 matrix with row stride `ld` elements; boxes of 64 cols x box_rows rows.
+bool encode_matrix(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(rows * ld * 2)};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_qkv_rope(QkvRopeParams& p, const void* x, const void* w, int64_t x_ld, cudaStream_t s,
+                            const char** why)
+{
+    if (!encode_matrix(&p.xmap, x, p.M, p.C, x_ld, QBM) || !encode_matrix(&p.wmap, w, 3LL * p.H * 128, p.C, p.C, QBN)) {
+        *why = "cuTensorMapEncodeTiled failed for x or w_qkv";
+        return cudaErrorInvalidValue;
+    }
+    static std::atomic<uint64_t> attr_set{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = uint64_t(1) << (dev & 63);
+    if (!(attr_set.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(qkv_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(QSMEM_BYTES));
+        if (e != cudaSuccess) {
+            *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+            return e;
+        }
+        attr_set.fetch_or(bit);
+    }
+    dim3 grid(static_cast<unsigned>((p.M + QBM - 1) / QBM), static_cast<unsigned>(3 * p.H * 128 / QBN));
+    qkv_rope_kernel<<<grid, QTHREADS, QSMEM_BYTES, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace sdv2

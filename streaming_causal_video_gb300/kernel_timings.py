@@ -1,0 +1,142 @@
+"""Per-entry-point timings at the workload shapes (CUDA events on the launch stream).
+
+For each HBM-bound call: algorithmic bytes per call, mean time over repeated calls on buffers
+larger than L2 (several distinct layer caches are cycled), achieved GB/s and the fraction of
+the copy-bandwidth peak.  For attention: flops per call and TFLOP/s.  Prints one JSON line per
+measurement.  Run: python -m streaming_causal_video_gb300.kernel_timings [--peak-gbs X]
+"""
+import argparse
+import json
+import os
+import sys
+
+import torch
+
+from . import _binding as sd
+from .layer import StreamSession
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+from synth_inputs import WORKLOADS, motion_frames_host, stream_config_dict  # noqa: E402
+
+
+def _time(fn, reps, stream):
+    for _ in range(3):
+        fn(0)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    stream.synchronize()
+    e0.record(stream)
+    for i in range(reps):
+        fn(i)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--peak-gbs", type=float, default=0.0, help="HBM peak (GB/s); default: MEASURED_PEAKS.json or 6800")
+    ap.add_argument("--layers", type=int, default=8, help="distinct layer caches cycled (more than L2 in total)")
+    args = ap.parse_args()
+    peak = args.peak_gbs
+    src = "given"
+    if not peak:
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+                d = json.load(fh)
+            peak = float(d.get("hbm_gbs") or d["hbm"]["gbs"])
+            src = "measured"
+        except Exception:
+            peak, src = 6800.0, "fallback"
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    out = []
+
+    def report(name, workload, bytes_per_call=None, flops_per_call=None, ms=None, extra=None):
+        rec = {"entry_point": name, "workload": workload, "ms_per_call": round(ms, 5)}
+        if bytes_per_call:
+            gbs = bytes_per_call / (ms * 1e-3) / 1e9
+            rec.update({"bytes_per_call": int(bytes_per_call), "GB_per_s": round(gbs, 1),
+                        "frac_of_hbm_peak": round(gbs / peak, 3), "peak_GB_per_s": peak, "peak_source": src})
+        if flops_per_call:
+            rec.update({"flops_per_call": flops_per_call, "TFLOP_per_s": round(flops_per_call / (ms * 1e-3) / 1e12, 1)})
+        if extra:
+            rec.update(extra)
+        out.append(rec)
+        print(json.dumps(rec), flush=True)
+
+    # ---- 1.3B-480p: rope_append, re-rotation, sink update, attention
+    w = WORKLOADS["wan13b_480p"]
+    cfg = sd.StreamConfig.make(**stream_config_dict(w))
+    nl = args.layers
+    sess = StreamSession(cfg, nl, w.start_frames, dev, stream)
+    g = torch.Generator(device=dev).manual_seed(1)
+    qkv = [tuple(torch.randn((1, w.nq, w.heads, 128), generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+           for _ in range(nl)]
+    steady = 6
+    for c in range(steady + 1):
+        for l in range(nl):
+            sess.layer_step(l, [c], *qkv[l], stream=stream)
+    stream.synchronize()
+
+    def rope(i):
+        l = i % nl
+        L = sess.layers[l]
+        sd.rope_append_kv(cfg, w.start_frames, [steady], *qkv[l], sess.q_rot, L.k, L.v, L.meta, sess.ws, stream)
+    report("sdv2_rope_append_kv", w.name, bytes_per_call=w.nq * w.heads * 1536, ms=_time(rope, 60, stream))
+
+    def attn(i):
+        L = sess.layers[i % nl]
+        sd.chunk_attention(cfg, [steady], sess.q_rot, L.k, L.v, sess.out, sess.ws, stream=stream)
+    nkv = sd.visible_tokens(cfg, steady)
+    report("sdv2_chunk_attention", w.name, flops_per_call=4.0 * w.heads * 128 * w.nq * nkv, ms=_time(attn, 30, stream),
+           extra={"kv_splits": sd.last_kv_splits()})
+
+    # re-rotation at a refresh chunk: every window slot holds an earlier frame (R = 7 chunks so
+    # that chunk 7 is a refresh chunk); time-axis vectors of the window keys are read and written
+    cfg_r = sd.StreamConfig.make(**stream_config_dict(w))
+    cfg_r.refresh_chunks = 7
+    tvecs = (w.rope_t // 2 + 3) // 4
+    rr_bytes = w.window_frames * w.hw * w.heads * tvecs * 16 * 2
+
+    def rerot(i):
+        L = sess.layers[i % nl]
+        sd.rope_refresh_rerotate(cfg_r, [7], L.k, L.meta, stream)
+    report("sdv2_rope_refresh_rerotate", w.name + " (window of 18 frames)", bytes_per_call=rr_bytes,
+           ms=_time(rerot, 60, stream))
+
+    sink_bytes = w.sink_frames * w.hw * w.heads * 256 * 2 * 2
+
+    def sink(i):
+        L = sess.layers[i % nl]
+        sd.sink_update(cfg, [steady], [1], L.k, L.v, L.meta, stream)
+    report("sdv2_sink_update", w.name + " (3 sink frames)", bytes_per_call=sink_bytes, ms=_time(sink, 60, stream))
+    del sess, qkv
+    torch.cuda.empty_cache()
+
+    # ---- stream batch: motion over 4 x 501 frames of 480x832x3, then the noise controller
+    wb = WORKLOADS["stream_batch"]
+    hp, wp, ch = wb.motion_frame_shape
+    frames = motion_frames_host(wb.batch, 501, hp, wp, ch, seed=wb.seed, device=dev)
+    ssd = torch.empty((wb.batch, 500), dtype=torch.int64, device=dev)
+    m = torch.empty((wb.batch, 500), dtype=torch.float32, device=dev)
+
+    def motion(i):
+        sd.motion_l2(frames, ssd, m, stream)
+    report("sdv2_motion_l2", "stream_batch: 4 x 501 frames of 480x832x3", bytes_per_call=frames.numel(),
+           ms=_time(motion, 10, stream))
+    ctl = sd.NoiseCtl(motion_lo=2.0, motion_hi=12.0, rate_lo=0.1, rate_hi=0.9, ema=0.5, more_noise_when_fast=1)
+    rate = torch.empty_like(m)
+
+    def noise(i):
+        sd.noise_from_motion(ctl, m, rate, None, stream)
+    report("sdv2_noise_from_motion", "stream_batch: 4 x 500 motion values", ms=_time(noise, 100, stream))
+    return out
+
+
+if __name__ == "__main__":
+    main()

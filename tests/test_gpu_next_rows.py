@@ -92,3 +92,93 @@ def test_noise_controller_bit_exact(fast_more, ema):
         ref = oracle.noise(m[:, part], 2.0, 12.0, 0.1, 0.9, ema, fast_more, state=st_o)
         np.testing.assert_array_equal(rp.cpu().numpy(), ref)
     np.testing.assert_array_equal(state.cpu().numpy(), st_o)
+
+
+# ------------------------------------------------------------------------------------------
+# fused QKV projection + Causal-RoPE + cache append
+# ------------------------------------------------------------------------------------------
+
+import math  # noqa: E402
+
+from gpu_common import config, to_f64, MAX_ABS, MEAN_ABS  # noqa: E402
+
+
+def _proj_inputs(w, c, seed=0):
+    C = w.heads * w.head_dim
+    g = torch.Generator().manual_seed(1000 * seed + c)
+    x = torch.randn((w.batch, w.nq, C), generator=g).to(torch.bfloat16)
+    W = (torch.randn((3 * C, C), generator=g) / math.sqrt(C)).to(torch.bfloat16)
+    bias = (torch.randn(3 * C, generator=g) * 0.1).float()
+    return x, W, bias
+
+
+def _close(got, ref, what):
+    """bf16 outputs against fp64: each element within 2^-8 of its rotation pair's norm (one bf16
+    rounding of a value no larger than that norm, plus fp32 accumulation error far below it)."""
+    pn = np.repeat(np.hypot(ref[..., 0::2], ref[..., 1::2]), 2, axis=-1)
+    err = np.abs(got - ref)
+    bad = err > 2.0 ** -8 * pn + 1e-6
+    assert not bad.any(), "%s: %d elements off, worst %.3g (pair norm %.3g)" % (
+        what, int(bad.sum()), float(err[bad].max()), float(pn[bad][np.argmax(err[bad])]))
+
+
+def _fused_reference(w, start, c, x_b, W, bias):
+    C = w.heads * w.head_dim
+    y = oracle.qkv_project(bits(x_b), bits(W), bias.numpy())          # [Nq][3C]
+    t, h, ww, frame = oracle.chunk_positions(start, c, w.chunk_frames, w.grid_h, w.grid_w, w.refresh_chunks)
+    rep = lambda a: np.repeat(a.astype(np.float64), w.heads)
+    rot = lambda z: oracle.rope_ideal(z.reshape(-1, w.head_dim), rep(t), rep(h), rep(ww), w.rope_t, w.rope_h,
+                                      w.rope_w, w.rope_base).reshape(w.nq, w.heads, w.head_dim)
+    q = rot(y[:, :C])
+    k = rot(y[:, C:2 * C])
+    v = y[:, 2 * C:].reshape(w.nq, w.heads, w.head_dim)
+    return q, k, v, t, frame
+
+
+@pytest.mark.parametrize("name,over,chunks,attend", [
+    ("tiny", dict(heads=2, window_frames=4, refresh_chunks=3, batch=2, start_frames=[0, 500]), 7, True),
+    ("wan13b_480p", dict(), 2, False),
+])
+def test_fused_qkv_rope_append_matches_fp64(name, over, chunks, attend):
+    w = small_workload(WORKLOADS[name], **over)
+    cfg = config(w)
+    starts = list(w.start_frames)
+    sess = sd.StreamSession(cfg, 1, starts, "cuda")
+    L = sess.layers[0]
+    hw = w.hw
+    kept = [{} for _ in range(w.batch)]        # per stream: frame -> (k_ref, v_ref) of retained frames
+    for c in range(chunks):
+        x, W, bias = _proj_inputs(w, c)
+        sd.qkv_rope_append(cfg, starts, [c] * w.batch, x.cuda(), W.cuda(), sess.q_rot, L.k, L.v, L.meta, sess.ws,
+                           bias=bias.cuda())
+        torch.cuda.synchronize()
+        qg = to_f64(sess.q_rot)                  # [B][H][Nq][D]
+        kg, vg = to_f64(L.k), to_f64(L.v)        # [B][H][rows][D]
+        meta = L.meta.cpu().numpy()
+        refs = []
+        for b in range(w.batch):
+            q, k, v, t, frame = _fused_reference(w, starts[b], c, x[b], W, bias)
+            refs.append(q)
+            _close(qg[b].transpose(1, 0, 2), q, "q_rot stream %d" % b)
+            for i in range(w.chunk_frames):
+                f = c * w.chunk_frames + i
+                s = oracle.slot_of_frame(f, w.sink_frames, w.window_frames)
+                assert tuple(meta[b, s]) == (f, int(t[i * hw])), (b, s, tuple(meta[b, s]))
+                _close(kg[b][:, s * hw:(s + 1) * hw, :].transpose(1, 0, 2), k[i * hw:(i + 1) * hw], "k slot %d" % s)
+                _close(vg[b][:, s * hw:(s + 1) * hw, :].transpose(1, 0, 2), v[i * hw:(i + 1) * hw], "v slot %d" % s)
+                kept[b][f] = (k[i * hw:(i + 1) * hw], v[i * hw:(i + 1) * hw])
+        if attend:
+            lse = torch.empty((w.batch, w.heads, w.nq), dtype=torch.float32, device="cuda")
+            sd.chunk_attention(cfg, [c] * w.batch, sess.q_rot, L.k, L.v, sess.out, sess.ws, lse=lse)
+            torch.cuda.synchronize()
+            out = to_f64(sess.out)
+            for b in range(w.batch):
+                n = (c + 1) * w.chunk_frames
+                fr = list(range(min(w.sink_frames, n))) + \
+                    [f for f in range(w.sink_frames, n)][-w.window_frames:]
+                for hh in range(w.heads):
+                    K = np.concatenate([kept[b][f][0][:, hh, :] for f in fr])
+                    V = np.concatenate([kept[b][f][1][:, hh, :] for f in fr])
+                    ref, _ = oracle.attention_f64(refs[b][:, hh, :], K, V, 1 / math.sqrt(w.head_dim))
+                    err = np.abs(out[b, :, hh, :] - ref)
+                    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (c, b, hh, err.max(), err.mean())

@@ -123,3 +123,16 @@ def test_noise_smoothing_closed_form_and_state_carry():
     a = oracle.noise(m[:, :10], **NOISE, ema=ema, more_noise_when_fast=1, state=state)
     b = oracle.noise(m[:, 10:], **NOISE, ema=ema, more_noise_when_fast=1, state=state)
     np.testing.assert_array_equal(np.concatenate([a, b], 1), oracle.noise(m, **NOISE, ema=ema, more_noise_when_fast=1))
+
+
+def test_qkv_projection_brute_force():
+    rng = np.random.default_rng(3)
+    x = oracle.f32_to_bf16(rng.standard_normal((3, 5)).astype(np.float32))
+    w = oracle.f32_to_bf16(rng.standard_normal((7, 5)).astype(np.float32))
+    bias = rng.standard_normal(7).astype(np.float32)
+    y = oracle.qkv_project(x, w, bias)
+    xf, wf = bf16_bits_to_f32(x), bf16_bits_to_f32(w)
+    for i in range(3):
+        for j in range(7):
+            ref = sum(float(xf[i, c]) * float(wf[j, c]) for c in range(5)) + float(bias[j])
+            assert y[i, j] == pytest.approx(ref, rel=1e-14, abs=1e-14)
