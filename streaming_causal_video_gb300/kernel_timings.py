@@ -115,6 +115,35 @@ def main():
         L = sess.layers[i % nl]
         sd.sink_update(cfg, [steady], [1], L.k, L.v, L.meta, stream)
     report("sdv2_sink_update", w.name + " (3 sink frames)", bytes_per_call=sink_bytes, ms=_time(sink, 60, stream))
+    # fused QKV projection + RoPE + append vs the unfused sequence (projection GEMM through
+    # torch/cuBLAS to bf16, then sdv2_rope_append_kv)
+    C = w.heads * w.head_dim
+    xs = [torch.randn((1, w.nq, C), generator=g, device=dev).to(torch.bfloat16) for _ in range(nl)]
+    Wq = (torch.randn((3 * C, C), generator=g, device=dev) / C ** 0.5).to(torch.bfloat16)
+    bq = torch.randn(3 * C, generator=g, device=dev).float() * 0.1
+    gemm_flops = 2.0 * w.nq * 3 * C * C
+
+    def fused(i):
+        L = sess.layers[i % nl]
+        sd.qkv_rope_append(cfg, w.start_frames, [steady], xs[i % nl], Wq, sess.q_rot, L.k, L.v, L.meta, sess.ws,
+                           bias=bq, stream=stream)
+    ms_f = _time(fused, 60, stream)
+    report("sdv2_qkv_rope_append", w.name + " (x [4680][1536] @ W[4608][1536]^T + bias, RoPE, append)",
+           flops_per_call=gemm_flops, ms=ms_f,
+           extra={"bytes_min": int((w.nq * C + 3 * C * C) * 2 + w.nq * 3 * C * 2)})
+    ybuf = torch.empty((1, w.nq, 3 * C), dtype=torch.bfloat16, device=dev)
+
+    def unfused(i):
+        l = i % nl
+        L = sess.layers[l]
+        torch.matmul(xs[l][0], Wq.t(), out=ybuf[0])
+        ybuf.add_(bq.to(torch.bfloat16))
+        y = ybuf.view(1, w.nq, 3, w.heads, w.head_dim)
+        cfg_s = sd.StreamConfig.make(**stream_config_dict(w, qkv_token_stride=3 * C))
+        sd.rope_append_kv(cfg_s, w.start_frames, [steady], y[:, :, 0], y[:, :, 1], y[:, :, 2], sess.q_rot, L.k, L.v,
+                          L.meta, sess.ws, stream)
+    ms_u = _time(unfused, 60, stream)
+    report("unfused: torch.matmul (cuBLAS) + bias + sdv2_rope_append_kv", w.name, flops_per_call=gemm_flops, ms=ms_u)
     del sess, qkv
     torch.cuda.empty_cache()
 
