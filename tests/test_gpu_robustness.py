@@ -1,0 +1,127 @@
+"""Robustness of the CUDA path: checkpoint/resume of the stream state, guard bands around
+every buffer a call writes, and CUDA-graph capture of the per-layer calls."""
+import numpy as np
+import pytest
+import torch
+
+import streaming_causal_video_gb300 as sd
+from synth_inputs import WORKLOADS, qkv_chunk_host
+from gpu_common import bits, config, small_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build_library()
+
+
+W = small_workload(WORKLOADS["tiny"], batch=2, heads=2, grid_h=5, grid_w=7, window_frames=5, sink_frames=2,
+                   refresh_chunks=4, start_frames=[3, 9000])
+
+
+def _inputs(c):
+    return tuple(t.cuda() for t in qkv_chunk_host(W, W.batch, c, seed_offset=5))
+
+
+def test_checkpoint_resume_is_bit_exact():
+    """The stream state is the cache, its metadata and (S, c): restoring a snapshot into a fresh
+    session and continuing gives the same outputs as never stopping."""
+    cfg = config(W)
+    a = sd.StreamSession(cfg, 1, W.start_frames, "cuda")
+    outs_a = []
+    snap = None
+    for c in range(9):
+        a.layer_step(0, [c, c], *_inputs(c))
+        if c == 4:
+            L = a.layers[0]
+            snap = (L.k.clone(), L.v.clone(), L.meta.clone())
+        if c > 4:
+            outs_a.append(bits(a.out).copy())
+    b = sd.StreamSession(cfg, 1, W.start_frames, "cuda")
+    Lb = b.layers[0]
+    Lb.k.copy_(snap[0]); Lb.v.copy_(snap[1]); Lb.meta.copy_(snap[2])
+    for i, c in enumerate(range(5, 9)):
+        b.layer_step(0, [c, c], *_inputs(c))
+        np.testing.assert_array_equal(bits(b.out), outs_a[i])
+    np.testing.assert_array_equal(bits(Lb.k), bits(a.layers[0].k))
+    np.testing.assert_array_equal(Lb.meta.cpu().numpy(), a.layers[0].meta.cpu().numpy())
+
+
+def _guarded(shape, dtype, fill):
+    """A tensor view with a canary band of 4096 bytes on both sides."""
+    pad = 4096 // torch.tensor([], dtype=dtype).element_size()
+    n = int(np.prod(shape))
+    base = torch.full((n + 2 * pad,), fill, dtype=dtype, device="cuda")
+    return base, base[pad:pad + n].view(shape), pad
+
+
+def test_guard_bands_stay_untouched():
+    cfg = config(W)
+    B, H, nq, D = W.batch, W.heads, W.nq, 128
+    rows = W.slots * W.hw
+    ws_b, ws, wp = _guarded((sd.workspace_bytes(cfg),), torch.uint8, 0xA5)
+    ws.zero_()
+    sd.workspace_init(cfg, ws)
+    bufs = {}
+    for name, shape in (("q_rot", (B, H, nq, D)), ("k", (B, H, rows, D)), ("v", (B, H, rows, D)),
+                        ("out", (B, nq, H, D))):
+        bufs[name] = _guarded(shape, torch.int16, 0x5A5A)
+    meta_b, meta, mp = _guarded((B, W.slots, 2), torch.int64, 0x1234567890)
+    lse_b, lse, lp = _guarded((B, H, nq), torch.float32, 7.25)
+    sd.cache_reset(cfg, bufs["k"][1], bufs["v"][1], meta)
+    frames_b, frames, fp_ = _guarded((2, 5, 16, 32, 3), torch.uint8, 0x33)
+    frames.copy_(torch.randint(0, 256, frames.shape, dtype=torch.uint8, device="cuda"))
+    ssd_b, ssd, sp = _guarded((2, 4), torch.int64, 0x77)
+    m_b, m, mp2 = _guarded((2, 4), torch.float32, 3.5)
+    for c in range(6):
+        q, k, v = _inputs(c)
+        sd.rope_append_kv(cfg, W.start_frames, [c, c], q, k, v, bufs["q_rot"][1], bufs["k"][1], bufs["v"][1], meta, ws)
+        sd.chunk_attention(cfg, [c, c], bufs["q_rot"][1], bufs["k"][1], bufs["v"][1], bufs["out"][1], ws, lse=lse)
+        if c % 4 == 0 and c > 0:
+            sd.rope_refresh_rerotate(cfg, [c, c], bufs["k"][1], meta)
+            sd.sink_update(cfg, [c, c], [1, 1], bufs["k"][1], bufs["v"][1], meta)
+    sd.motion_l2(frames, ssd, m)
+    torch.cuda.synchronize()
+    sd.check_device_error(ws)
+
+    def bands_ok(base, pad, fill):
+        h = base.cpu()
+        ref = torch.full((pad,), fill, dtype=base.dtype)
+        return torch.equal(h[:pad], ref) and torch.equal(h[-pad:], ref)
+    for name, (base, _, pad) in bufs.items():
+        assert bands_ok(base, pad, 0x5A5A), name
+    assert bands_ok(meta_b, mp, 0x1234567890)
+    assert bands_ok(lse_b, lp, 7.25)
+    assert bands_ok(ws_b, wp, 0xA5)
+    assert bands_ok(ssd_b, sp, 0x77)
+    assert bands_ok(m_b, mp2, 3.5)
+    assert bands_ok(frames_b, fp_, 0x33)
+
+
+def test_cuda_graph_replay_equals_eager():
+    """The per-layer calls (append + attention) launch kernels only, with their arguments in the
+    launch parameters, so a captured graph replays them exactly."""
+    cfg = config(W)
+    eager = sd.StreamSession(cfg, 1, W.start_frames, "cuda")
+    graphed = sd.StreamSession(cfg, 1, W.start_frames, "cuda")
+    for c in range(3):
+        eager.layer_step(0, [c, c], *_inputs(c))
+        graphed.layer_step(0, [c, c], *_inputs(c))
+    q, k, v = _inputs(3)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        graphed.layer_step(0, [3, 3], q, k, v, stream=s)
+    g.replay()
+    eager.layer_step(0, [3, 3], q, k, v)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(graphed.out), bits(eager.out))
+    np.testing.assert_array_equal(bits(graphed.layers[0].k), bits(eager.layers[0].k))
+    g.replay()                              # a second replay (the next denoise step) is idempotent
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(graphed.out), bits(eager.out))
