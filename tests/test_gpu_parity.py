@@ -238,6 +238,40 @@ def test_forced_kv_splits_all_match_oracle(chunk_stop):
         sd.debug_set_kv_splits(0)
 
 
+GROW = small_workload(WORKLOADS["tiny"], heads=2, grid_h=8, grid_w=16, chunk_frames=1, sink_frames=1,
+                      window_frames=3, chunks=4)
+
+
+def test_scores_growing_across_key_tiles():
+    """Each later frame's keys are scaled up (x0.05, x1, x4, x16), so the running row max jumps
+    by far more than the lazy-rescale threshold from one 128-key tile to the next; a third of the
+    query rows are scaled down so that only some rows of a warp jump.  Every result matches the
+    oracle with 1, 2 and 3 key splits."""
+    w = GROW
+    g = torch.Generator().manual_seed(21)
+    shape = (1, w.nq, w.heads, 128)
+    row_scale = torch.where(torch.arange(w.nq) % 3 == 0, 0.02, 1.0).reshape(1, w.nq, 1, 1)
+    ls = LockStep(w)
+    for c, ks in enumerate((0.05, 1.0, 4.0, 16.0)):
+        q = (torch.randn(shape, generator=g) * row_scale).to(torch.bfloat16)
+        k = (torch.randn(shape, generator=g) * ks).to(torch.bfloat16)
+        v = torch.randn(shape, generator=g).to(torch.bfloat16)
+        q_rot_o = ls.step([c], qkv=(q, k, v))
+        ls.check_attention(q_rot_o)
+    try:
+        for splits in (1, 2, 3):
+            sd.debug_set_kv_splits(splits)
+            L = ls.sess.layers[0]
+            sd.chunk_attention(ls.cfg, [w.chunks - 1], ls.sess.q_rot, L.k, L.v, ls.sess.out, ls.sess.ws,
+                               lse=ls.lse)
+            torch.cuda.synchronize()
+            assert sd.last_kv_splits() == splits
+            ls.check_attention(q_rot_o)
+        sd.check_device_error(ls.sess.ws)
+    finally:
+        sd.debug_set_kv_splits(0)
+
+
 # ------------------------------------------------------------------------------------------
 # full workload shapes, in the launch configuration the bench times (sampled rows)
 # ------------------------------------------------------------------------------------------
