@@ -149,9 +149,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
     if (warp == TMA_WARP || warp == TMA_V_WARP) {
         // ------------------------------------------------------------------ producers (TMA)
         // One thread loads Q and the K ring, another the V ring, so that a late K slot never
-        // holds back a V load.  Each also prefetches its tiles PREFETCH_TILES ahead into L2:
-        // the CTAs of one head walk the same keys in step, so without it every tile would be a
-        // DRAM-latency load.
+        // holds back a V load.  Every fourth query pair of a head also prefetches the tiles
+        // PREFETCH_TILES ahead into L2: the CTAs of one head walk the same keys in step, so
+        // without it every tile would be a DRAM-latency load, and one prefetching CTA in four
+        // is enough to keep the others hitting in L2.
         if (lane == 0) {
             const bool is_k = (warp == TMA_WARP);
             const CUtensorMap* map = is_k ? &p.kmap[b] : &p.vmap[b];
@@ -170,7 +171,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                     for (int hf = 0; hf < 2; ++hf)
                         tma_load_3d(sQ + t * TILE + hf * HALF, qm, BAR(B_QFULL), hf * 64, q0 + t * BM, plane);
             }
-            for (int j = 0; j < PREFETCH_TILES && j < ntiles; ++j)
+            const bool do_pf = (qp % 4) == 0;   // every fourth query pair prefetches
+            for (int j = 0; do_pf && j < PREFETCH_TILES && j < ntiles; ++j)
                 for (int hf = 0; hf < 2; ++hf) tma_prefetch_l2_3d(map, hf * 64, (t_begin + j) * BN, h);
             int pend[NST] = {};
             uint32_t par[NST] = {};
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                 const uint32_t ph = static_cast<uint32_t>(j / nst) & 1u;
                 if (!mbar_wait_bounded(BAR(bar_empty + st), ph ^ 1u, tmo, abort_flag)) { raise_abort(abort_flag, p.err); break; }
                 const int jg = t_begin + j;
-                if (j + PREFETCH_TILES < ntiles)
+                if (do_pf && j + PREFETCH_TILES < ntiles)
                     for (int hf = 0; hf < 2; ++hf) tma_prefetch_l2_3d(map, hf * 64, (jg + PREFETCH_TILES) * BN, h);
                 if (jg != p.drop_tile) {
                     mbar_arrive_expect_tx(BAR(bar_full + st), TILE);
@@ -198,8 +200,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------------ MMA issuer
-        // The whole warp runs this loop converged; lane 0 does the barrier waits and broadcasts
-        // the outcome, one elected lane issues each tcgen05 instruction.  Shared-memory
+        // The whole warp runs this loop converged: every lane polls each barrier and a warp
+        // vote agrees on the outcome (cheaper than one lane polling while the others wait at a
+        // shuffle), and one elected lane issues each tcgen05 instruction.  Shared-memory
         // descriptors are built once: the k-th 16-wide step of a K-major 128-byte-swizzled tile
         // starts (k/4)*HALF + (k%4)*32 bytes further, and V's k-th step 16 rows (2048 bytes)
         // further, which is a constant added to the descriptor's address field.
@@ -210,9 +213,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
         const uint64_t dV = sdesc_sw128(sV, HALF, 1024);
         constexpr uint64_t kTileStep = TILE >> 4;           // descriptor units (16 bytes)
         auto wait = [&](int bar_idx, uint32_t parity) -> bool {
-            int r = 1;
-            if (lane == 0) r = mbar_wait_bounded(BAR(bar_idx), parity, tmo, abort_flag) ? 1 : 0;
-            return __shfl_sync(0xffffffffu, r, 0) != 0;
+            const bool r = mbar_wait_bounded(BAR(bar_idx), parity, tmo, abort_flag);
+            return __all_sync(0xffffffffu, r);
         };
         auto issue_s = [&](int t, int ks) {
             const uint64_t a0 = dQ + static_cast<uint64_t>(t) * kTileStep;
