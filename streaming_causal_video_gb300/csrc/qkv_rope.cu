@@ -13,7 +13,8 @@
 // hidden dimension in steps of 64 (128-byte swizzled TMA boxes), through a 2-stage ring
 // (48 KB per stage), so that two CTAs share an SM and one's epilogue overlaps the other's main
 // loop.  The accumulator (128 lanes x 256 fp32 columns) lives in tensor memory.
-//   warp 0: TMA producer; warp 1: MMA issuer (converged, elect.sync); warps 2-5: epilogue,
+//   warp 0: TMA producer; warp 1: MMA issuer (converged: every lane polls the stage barrier and
+//   a warp vote agrees on the outcome; elect.sync issues); warps 2-5: epilogue,
 //   thread = token row = TMEM lane.
 // Rounding: acc (fp32, fp32 accumulation) + bias (fp32 add); q and k pairs rotated in fp32 as
 // (fmaf(x, c, -(y*s)), fmaf(x, s, y*c)); one bf16 round-to-nearest-even per output.
@@ -117,9 +118,8 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
         bool ok = true;
         for (int kk = 0; kk < ksteps; ++kk) {
             const int st = kk % QST;
-            int r = 1;
-            if (lane == 0) r = mbar_wait_bounded(QBAR(st), static_cast<uint32_t>(kk / QST) & 1u, tmo, abort_flag) ? 1 : 0;
-            if (!__shfl_sync(0xffffffffu, r, 0)) {
+            const bool r = mbar_wait_bounded(QBAR(st), static_cast<uint32_t>(kk / QST) & 1u, tmo, abort_flag);
+            if (!__all_sync(0xffffffffu, r)) {
                 ok = false;
                 break;
             }
