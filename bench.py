@@ -438,12 +438,22 @@ def run_ours(args, dist):
     return res
 
 
-def cpu_baseline_entry(w, seconds=12.0):
+def cpu_baseline_entry(w, seconds=12.0, single_seconds=4.0):
+    """The oracle on all host cores (the reported value) and, for scale, on one thread."""
+    import oracle
     flops, secs, rows, threads = oracle_sample(w, seconds)
+    all_threads = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        f1, s1, r1, _ = oracle_sample(w, single_seconds, seed=1, max_rows=256)
+    finally:
+        oracle.set_num_threads(all_threads)
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "single_thread_value": round(f1 / s1 / 1e12, 7),
             "sample": "fp64 oracle attention of %d query rows against the steady-state %d keys of one head "
-                      "(bf16 inputs), %.1f s; TFLOP/s counts the same 4*D*Nkv flops per row as the GPU metric"
-                      % (rows, w.slots * w.hw, secs)}
+                      "(bf16 inputs), %.1f s on %d threads; single_thread_value: %d rows, %.1f s on 1 thread; "
+                      "TFLOP/s counts the same 4*D*Nkv flops per row as the GPU metric"
+                      % (rows, w.slots * w.hw, secs, threads, r1, s1)}
 
 
 def run_reference(args, dist):
