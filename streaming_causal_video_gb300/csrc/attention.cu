@@ -394,17 +394,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
         } else {
             // Split keys: publish this split's unnormalised rows, then the last split to arrive
             // for this item merges all of them (no CTA waits for another).
+            // Partial rows are stored as groups of four dims, [split item][HD/4][row][4] floats,
+            // so that the 32 rows of a warp write (and the merge reads) 512 contiguous bytes.
             const int64_t slot = (item * p.splits + sp) * kAttnRowsPerCta + rloc;
             if (ok) {
-                float4* po = reinterpret_cast<float4*>(p.part_o + slot * HD);
+                float4* po = reinterpret_cast<float4*>(p.part_o) + (item * p.splits + sp) * (HD / 4) * kAttnRowsPerCta + rloc;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
                     tmem_ld_x32_sync(tO + c * 32, o);
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
-                        __stcg(po + c * 8 + v, make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                                           __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
+                        __stcg(po + (c * 8 + v) * kAttnRowsPerCta,
+                               make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                           __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
                 }
                 __stcg(reinterpret_cast<float2*>(p.part_ml) + slot, make_float2(m_run, l_run));
             }
@@ -444,25 +447,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                 const float inv = 1.0f / L;
                 if (q < p.Nq) {
                     uint16_t* dst = p.out + ((static_cast<int64_t>(b) * p.Nq + q) * p.H + h) * HD;
+                    // 32 dims at a time: the eight float4 loads of one split are issued together.
 #pragma unroll 1
-                    for (int c = 0; c < HD / 8; ++c) {
-                        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    for (int c = 0; c < HD / 32; ++c) {
+                        float4 acc[8];
 #pragma unroll
-                        for (int s2 = 0; s2 < kMaxKvSplits; ++s2) {
-                            if (s2 < p.splits) {
-                                const float4* src = reinterpret_cast<const float4*>(
-                                    p.part_o + ((item * p.splits + s2) * kAttnRowsPerCta + rloc) * HD + c * 8);
-                                const float4 u = __ldcg(src), w2 = __ldcg(src + 1);
-                                acc[0] += u.x * ms[s2]; acc[1] += u.y * ms[s2]; acc[2] += u.z * ms[s2]; acc[3] += u.w * ms[s2];
-                                acc[4] += w2.x * ms[s2]; acc[5] += w2.y * ms[s2]; acc[6] += w2.z * ms[s2]; acc[7] += w2.w * ms[s2];
+                        for (int v = 0; v < 8; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+                        for (int s2 = 0; s2 < p.splits; ++s2) {
+                            const float4* src = reinterpret_cast<const float4*>(p.part_o) +
+                                                ((item * p.splits + s2) * (HD / 4) + c * 8) * kAttnRowsPerCta + rloc;
+                            float4 u[8];
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) u[v] = __ldcg(src + v * kAttnRowsPerCta);
+                            const float wgt = ms[s2 < kMaxKvSplits ? s2 : 0];
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                acc[v].x += u[v].x * wgt; acc[v].y += u[v].y * wgt;
+                                acc[v].z += u[v].z * wgt; acc[v].w += u[v].w * wgt;
                             }
                         }
-                        uint4 wv;
-                        wv.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-                        wv.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-                        wv.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-                        wv.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-                        *reinterpret_cast<uint4*>(dst + c * 8) = wv;
+#pragma unroll
+                        for (int v = 0; v < 8; v += 2) {
+                            uint4 wv;
+                            wv.x = pack_bf16x2(acc[v].x * inv, acc[v].y * inv);
+                            wv.y = pack_bf16x2(acc[v].z * inv, acc[v].w * inv);
+                            wv.z = pack_bf16x2(acc[v + 1].x * inv, acc[v + 1].y * inv);
+                            wv.w = pack_bf16x2(acc[v + 1].z * inv, acc[v + 1].w * inv);
+                            *reinterpret_cast<uint4*>(dst + c * 32 + v * 4) = wv;
+                        }
                     }
                     if (p.lse) p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + q] = (M + __log2f(L)) * kLn2;
                 }
