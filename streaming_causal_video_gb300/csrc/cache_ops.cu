@@ -29,65 +29,91 @@ __device__ __forceinline__ uint32_t rotate_pair_rr(uint32_t xy, float c, float s
     return *reinterpret_cast<const uint32_t*>(&o);
 }
 
-// One thread per (stream, window slot, token of the frame, head, 16-byte vector of the time
-// segment).  A slot qualifies when it holds a frame of an earlier chunk (0 <= frame_id < c*F)
-// of a stream whose current chunk is a refresh chunk.
-__global__ void rerotate_kernel(const __grid_constant__ RerotateParams p)
+// Re-rotation.  Grid: z = stream * W + window slot, y = head, x covers the slot's tokens; 8 lanes
+// per token row (16 when the time segment spans more than 8 vectors), lane v handles the row's
+// v-th 16-byte vector when v < tvecs (the time segment is the first tvecs vectors of the
+// 256-byte row); each thread takes four rows, loading all four before rotating.  A slot qualifies when it holds
+// a frame of an earlier chunk (0 <= frame_id < c*F) of a stream whose current chunk is a
+// refresh chunk.  No division anywhere: the rows of one (stream, head, slot) are contiguous.
+__host__ __device__ inline int rerotate_lane_shift(int tvecs) { return tvecs <= 8 ? 3 : 4; }
+constexpr int kRerotRowsPerThread = 4;
+
+__global__ void __launch_bounds__(256) rerotate_kernel(const __grid_constant__ RerotateParams p)
 {
-    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t per_slot = static_cast<int64_t>(p.HW) * p.H * p.tvecs;
-    const int64_t per_stream = per_slot * p.W;
-    if (gid >= per_stream * p.B) return;
-    const int b = static_cast<int>(gid / per_stream);
-    const int64_t rem = gid - static_cast<int64_t>(b) * per_stream;
-    const int ws = static_cast<int>(rem / per_slot);            // window slot index 0..W-1
-    const int64_t r2 = rem - static_cast<int64_t>(ws) * per_slot;
-    const int vec = static_cast<int>(r2 % p.tvecs);
-    const int64_t r3 = r2 / p.tvecs;
-    const int h = static_cast<int>(r3 % p.H);
-    const int tok = static_cast<int>(r3 / p.H);
-    if (!p.active[b]) return;
+    const int b = blockIdx.z / p.W;
+    const int ws = blockIdx.z - b * p.W;                        // window slot index 0..W-1
+    const int h = blockIdx.y;
+    const int lsh = rerotate_lane_shift(p.tvecs);
+    const int vec = threadIdx.x & ((1 << lsh) - 1);
+    if (!p.active[b] || vec >= p.tvecs) return;
     const int slot = p.Fs + ws;
     sdv2_slot_meta* m = p.meta + static_cast<int64_t>(b) * p.nslots + slot;
     const int64_t fid = m->frame_id;
     if (fid < 0 || fid >= p.limit[b]) return;
-    uint4* row = reinterpret_cast<uint4*>(
-        p.k_cache + ((static_cast<int64_t>(b) * p.H + h) * p.nslots * p.HW + static_cast<int64_t>(slot) * p.HW + tok) * 128);
-    uint4 v = row[vec];
-    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+    // this thread's rows: tok0 + k * (tokens covered by the block in one pass), k < 4
+    const int per_pass = 256 >> lsh;
+    const int tok0 = blockIdx.x * per_pass * kRerotRowsPerThread + (threadIdx.x >> lsh);
+    uint4* base = reinterpret_cast<uint4*>(p.k_cache + ((static_cast<int64_t>(b) * p.H + h) * p.nslots * p.HW +
+                                                        static_cast<int64_t>(slot) * p.HW) * 128);
+    uint4 v[kRerotRowsPerThread];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int pr = vec * 4 + u;
-        if (pr < p.tp) w[u] = rotate_pair_rr(w[u], p.cs[pr].x, p.cs[pr].y);
+    for (int k = 0; k < kRerotRowsPerThread; ++k) {
+        const int tok = tok0 + k * per_pass;
+        if (tok < p.HW) v[k] = base[static_cast<int64_t>(tok) * 16 + vec];
     }
-    row[vec] = v;
-    if (tok == 0 && h == 0 && vec == 0) m->tpos -= p.shift;   // frame_id, which the others read, stays
+#pragma unroll
+    for (int k = 0; k < kRerotRowsPerThread; ++k) {
+        const int tok = tok0 + k * per_pass;
+        if (tok < p.HW) {
+            uint32_t* w = reinterpret_cast<uint32_t*>(&v[k]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int pr = vec * 4 + u;
+                if (pr < p.tp) w[u] = rotate_pair_rr(w[u], p.cs[pr].x, p.cs[pr].y);
+            }
+            base[static_cast<int64_t>(tok) * 16 + vec] = v[k];
+        }
+    }
+    if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) m->tpos -= p.shift;   // frame_id, which the others read, stays
 }
 
-// One thread per (stream, sink slot, token, head, 16-byte vector) copies k and v rows; the
-// first thread of each slot copies the metadata.
-__global__ void sink_update_kernel(const __grid_constant__ SinkUpdateParams p)
+// Sink update.  Grid: z = stream * F_s + sink slot, y = head, x covers the slot's HW * 16
+// vectors of k and of v (contiguous for one (stream, head, slot)); each thread copies four
+// vectors of each, so that several loads are in flight.  The first thread of each slot copies
+// the metadata.
+constexpr int kSinkVecsPerThread = 4;
+__global__ void __launch_bounds__(256) sink_update_kernel(const __grid_constant__ SinkUpdateParams p)
 {
-    const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t per_slot = static_cast<int64_t>(p.HW) * p.H * 16;
-    const int64_t per_stream = per_slot * p.Fs;
-    if (gid >= per_stream * p.B) return;
-    const int b = static_cast<int>(gid / per_stream);
+    const int b = blockIdx.z / p.Fs;
+    const int s = blockIdx.z - b * p.Fs;
+    const int h = blockIdx.y;
     if (!p.active[b]) return;
-    const int64_t rem = gid - static_cast<int64_t>(b) * per_stream;
-    const int s = static_cast<int>(rem / per_slot);
-    const int64_t r2 = rem - static_cast<int64_t>(s) * per_slot;
-    const int vec = static_cast<int>(r2 & 15);
-    const int64_t r3 = r2 >> 4;
-    const int h = static_cast<int>(r3 % p.H);
-    const int tok = static_cast<int>(r3 / p.H);
     const int src = p.src_slot[b * kMaxSinkFrames + s];
     const int64_t head_base = (static_cast<int64_t>(b) * p.H + h) * p.nslots * p.HW;
-    const int64_t from = (head_base + static_cast<int64_t>(src) * p.HW + tok) * 16 + vec;
-    const int64_t to = (head_base + static_cast<int64_t>(s) * p.HW + tok) * 16 + vec;
-    reinterpret_cast<uint4*>(p.k_cache)[to] = reinterpret_cast<const uint4*>(p.k_cache)[from];
-    reinterpret_cast<uint4*>(p.v_cache)[to] = reinterpret_cast<const uint4*>(p.v_cache)[from];
-    if (tok == 0 && h == 0 && vec == 0)
+    const uint4* kf = reinterpret_cast<const uint4*>(p.k_cache) + (head_base + static_cast<int64_t>(src) * p.HW) * 16;
+    const uint4* vf = reinterpret_cast<const uint4*>(p.v_cache) + (head_base + static_cast<int64_t>(src) * p.HW) * 16;
+    uint4* kt = reinterpret_cast<uint4*>(p.k_cache) + (head_base + static_cast<int64_t>(s) * p.HW) * 16;
+    uint4* vt = reinterpret_cast<uint4*>(p.v_cache) + (head_base + static_cast<int64_t>(s) * p.HW) * 16;
+    const int n = p.HW * 16;
+    const int i0 = blockIdx.x * (256 * kSinkVecsPerThread) + threadIdx.x;
+    uint4 kv[kSinkVecsPerThread], vv[kSinkVecsPerThread];
+#pragma unroll
+    for (int u = 0; u < kSinkVecsPerThread; ++u) {
+        const int i = i0 + u * 256;
+        if (i < n) {
+            kv[u] = kf[i];
+            vv[u] = vf[i];
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kSinkVecsPerThread; ++u) {
+        const int i = i0 + u * 256;
+        if (i < n) {
+            kt[i] = kv[u];
+            vt[i] = vv[u];
+        }
+    }
+    if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0)
         p.meta[static_cast<int64_t>(b) * p.nslots + s] = p.meta[static_cast<int64_t>(b) * p.nslots + src];
 }
 
@@ -132,17 +158,20 @@ __global__ void __launch_bounds__(kNoiseThreads) noise_kernel(const __grid_const
 
 cudaError_t launch_rerotate(const RerotateParams& p, cudaStream_t s)
 {
-    const int64_t n = static_cast<int64_t>(p.B) * p.W * p.HW * p.H * p.tvecs;
-    if (n == 0) return cudaSuccess;
-    rerotate_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(p);
+    if (p.B == 0 || p.W == 0 || p.HW == 0 || p.H == 0 || p.tvecs == 0) return cudaSuccess;
+    const int tpb = (256 >> rerotate_lane_shift(p.tvecs)) * kRerotRowsPerThread;   // tokens per block
+    const dim3 grid(static_cast<unsigned>((p.HW + tpb - 1) / tpb), static_cast<unsigned>(p.H), static_cast<unsigned>(p.B * p.W));
+    rerotate_kernel<<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_sink_update(const SinkUpdateParams& p, cudaStream_t s)
 {
-    const int64_t n = static_cast<int64_t>(p.B) * p.Fs * p.HW * p.H * 16;
-    if (n == 0) return cudaSuccess;
-    sink_update_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(p);
+    if (p.B == 0 || p.Fs == 0 || p.HW == 0 || p.H == 0) return cudaSuccess;
+    const int per_block = 256 * kSinkVecsPerThread;
+    const dim3 grid(static_cast<unsigned>((p.HW * 16 + per_block - 1) / per_block), static_cast<unsigned>(p.H),
+                    static_cast<unsigned>(p.B * p.Fs));
+    sink_update_kernel<<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

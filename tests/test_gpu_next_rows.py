@@ -36,10 +36,13 @@ def _attend(ls, chunks):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("window,sink_updates", [(9, False), (9, True), (4, True)])
-def test_refresh_rerotation_and_sink_update_stream(window, sink_updates):
+@pytest.mark.parametrize("window,sink_updates,rope", [(9, False, (44, 42, 42)), (9, True, (44, 42, 42)),
+                                                     (4, True, (44, 42, 42)),
+                                                     # a time axis of 72 dims spans 9 of a row's 16-byte vectors
+                                                     (9, True, (72, 28, 28))])
+def test_refresh_rerotation_and_sink_update_stream(window, sink_updates, rope):
     w = small_workload(WORKLOADS["tiny"], batch=2, heads=2, window_frames=window, refresh_chunks=3,
-                       start_frames=[0, 777])
+                       start_frames=[0, 777], rope_t=rope[0], rope_h=rope[1], rope_w=rope[2])
     ls = LockStep(w)
     for c in range(11):
         chunks = [c, c]
