@@ -19,6 +19,7 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|referenc
 """
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -165,11 +166,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def attention_source_hash():
+def code_only(text):
+    """C/CUDA source without comments and with whitespace collapsed, so that an edit to comments
+    does not count as a change of the kernel."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def attention_source_hash(read=None):
+    """Hash of the code (not the comments) the attention kernel is built from."""
     h = hashlib.sha256()
     for f in ("attention.cu", "ptx.cuh", "tmem_io.cuh", "internal.h"):
-        with open(os.path.join(ROOT, "streaming_causal_video_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        if read is None:
+            with open(os.path.join(ROOT, "streaming_causal_video_gb300", "csrc", f)) as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(code_only(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -10,10 +10,12 @@
 //
 // How (one CTA = one head of one stream, two 128-row query tiles and one key split):
 //   warps 8, 10 (TMA): Q tiles once, then K (warp 8, 3-stage ring) and V (warp 10, 2-stage ring)
-//                       tiles of 128 keys, each prefetched into L2 four tiles ahead.  3D tensor
-//                       maps per stream clip the key range at the valid prefix, so rows past it
-//                       arrive as zeros; 128-byte swizzled boxes of 64 dims.
-//   warp 9 (MMA)      : runs converged; an elected lane issues each tcgen05.mma.  S_t = Q_t K^T
+//                       tiles of 128 keys; every fourth query pair of a head also prefetches them
+//                       into L2 four tiles ahead.  3D tensor maps per stream clip the key range at
+//                       the valid prefix, so rows past it arrive as zeros; 128-byte swizzled boxes
+//                       of 64 dims.
+//   warp 9 (MMA)      : runs converged: every lane polls each barrier and a warp vote agrees on
+//                       the outcome; an elected lane issues each tcgen05.mma.  S_t = Q_t K^T
 //                       (A and B from shared memory, K-major) into tensor memory;
 //                       O_t += P_t V (A = P from tensor memory, B = V from shared memory,
 //                       MN-major).  Completion is signalled with tcgen05.commit on mbarriers.
@@ -29,6 +31,11 @@
 // other tile's PV and next QK^T.  Because tcgen05 operations issued by one thread complete in
 // order and a commit covers all earlier ones, the arrival of S_t(j) also proves that
 // O_t += P_t(j-1) V(j-1) has finished, so O_t can be rescaled without another barrier.
+//
+// With several key splits, each split publishes its unnormalised rows and (max, sum) to the
+// workspace, stored as [dims/4][row][4] floats so that a warp moves 512 contiguous bytes; the
+// split that finishes last for a query pair (an atomic counter) merges them.  No CTA waits for
+// another.
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel records kErrTimeout in
 // the workspace error word, tells the other roles to stop, drains its own copies and MMAs and
