@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 import test_oracle_pins as P
+import test_oracle_pins_next as PN
 
 DT, DH, DW, BASE = P.DT, P.DH, P.DW, P.BASE
 
@@ -22,6 +23,9 @@ _slot_of_frame = oracle.slot_of_frame
 _attention_f64 = oracle.attention_f64
 _softmax = oracle.softmax
 _motion_ssd = oracle.motion_ssd
+_noise = oracle.noise
+_qkv_project = oracle.qkv_project
+_rope_spec = oracle.rope_spec
 
 
 # ------------------------------------------------------------------------------------------
@@ -190,6 +194,94 @@ MOTION_PINS = [P.test_motion_identical_frames_and_symmetry,
                lambda: P.test_motion_shifted_ramp_closed_form(3, 7)]
 
 
+# ------------------------------------------------------------------------------------------
+# next-row mutants: refresh re-rotation, sink update, noise map, projection
+# ------------------------------------------------------------------------------------------
+
+def _rerotate_with(shift_sign=-1, all_axes=False, lower_tpos=True):
+    def refresh_rerotate(self, chunk):
+        w = self.w
+        R = w.refresh_chunks
+        if not (R > 0 and chunk > 0 and chunk % R == 0):
+            return False
+        shift = w.chunk_frames * R
+        for e in self.cache.entries[w.sink_frames:]:
+            if 0 <= e[0] < chunk * w.chunk_frames:
+                n = e[2].shape[0]
+                z = np.zeros(n, np.int64)
+                d = np.full(n, shift_sign * shift, np.int64)
+                e[2] = _rope_spec(e[2], d, d if all_axes else z, d if all_axes else z, w.rope_t, w.rope_h,
+                                  w.rope_w, w.rope_base)
+                if lower_tpos:
+                    e[1] -= shift
+        return True
+    return refresh_rerotate
+
+
+def sink_update_oldest(self):
+    fs = self.w.sink_frames
+    first = self.cache.entries[fs:2 * fs]
+    self.cache.entries[:fs] = [[e[0], e[1], e[2].copy(), e[3].copy()] for e in first]
+
+
+def sink_update_aliased(self):
+    fs = self.w.sink_frames
+    self.cache.entries[:fs] = [[e[0], e[1], e[2], e[3]] for e in self.cache.entries[-fs:]]
+
+
+def noise_direction_inverted(m, m_lo, m_hi, out_lo, out_hi, ema, more_noise_when_fast, state=None):
+    return _noise(m, m_lo, m_hi, out_lo, out_hi, ema, 1 - int(more_noise_when_fast), state)
+
+
+def noise_state_ignored(m, m_lo, m_hi, out_lo, out_hi, ema, more_noise_when_fast, state=None):
+    return _noise(m, m_lo, m_hi, out_lo, out_hi, ema, more_noise_when_fast, None)
+
+
+def qkv_bias_twice(x_bits, w_bits, bias=None):
+    y = _qkv_project(x_bits, w_bits, bias)
+    return y if bias is None else y + np.asarray(bias, np.float32).astype(np.float64)[None, :]
+
+
+def qkv_bias_dropped(x_bits, w_bits, bias=None):
+    return _qkv_project(x_bits, w_bits, None)
+
+
+REROTATE_PINS = [PN.test_stream_tpos_after_resets_equals_continuous_tpos_minus_shifts,
+                 PN.test_stream_rerotated_keys_keep_scores_continuous]
+NOISE_PINS = [lambda: PN.test_noise_map_monotone_endpoints_and_direction(0),
+              lambda: PN.test_noise_map_monotone_endpoints_and_direction(1),
+              PN.test_noise_smoothing_closed_form_and_state_carry]
+
+NEXT_MUTANTS = [
+    ("rerotation: keys turned forward instead of back", oracle.StreamOracle, "refresh_rerotate",
+     _rerotate_with(shift_sign=+1), REROTATE_PINS),
+    ("rerotation: all three axes turned", oracle.StreamOracle, "refresh_rerotate",
+     _rerotate_with(all_axes=True), REROTATE_PINS),
+    ("rerotation: time index not lowered", oracle.StreamOracle, "refresh_rerotate",
+     _rerotate_with(lower_tpos=False), REROTATE_PINS),
+    ("sink update: oldest window frames copied", oracle.StreamOracle, "sink_update", sink_update_oldest,
+     [PN.test_sink_update_copies_the_last_frames]),
+    ("sink update: arrays shared instead of copied", oracle.StreamOracle, "sink_update", sink_update_aliased,
+     [PN.test_sink_update_copies_the_last_frames]),
+    ("noise: direction flag inverted", oracle, "noise", noise_direction_inverted, NOISE_PINS),
+    ("noise: smoothing state not carried", oracle, "noise", noise_state_ignored, NOISE_PINS),
+    ("projection: bias added twice", oracle, "qkv_project", qkv_bias_twice, [PN.test_qkv_projection_brute_force]),
+    ("projection: bias dropped", oracle, "qkv_project", qkv_bias_dropped, [PN.test_qkv_projection_brute_force]),
+]
+
+
+@pytest.mark.parametrize("name,owner,attr,mutant,pins", NEXT_MUTANTS, ids=[m[0] for m in NEXT_MUTANTS])
+def test_next_row_pins_reject_mutant(monkeypatch, name, owner, attr, mutant, pins):
+    monkeypatch.setattr(owner, attr, mutant)
+    failed = 0
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, "no pin caught the mutant: " + name
+
+
 MUTANTS = [
     ("rope: negated angle", "rope_ideal", rope_negated_angle, ROPE_PINS),
     ("rope: h and w positions swapped", "rope_ideal", rope_h_w_swapped, ROPE_PINS),
@@ -229,6 +321,6 @@ def test_pins_reject_mutant(monkeypatch, name, target, mutant, pins):
 
 
 def test_unmutated_oracle_passes_the_same_pins():
-    for pins in (ROPE_PINS, POSITION_PINS, CACHE_PINS, ATTENTION_PINS, MOTION_PINS):
+    for pins in (ROPE_PINS, POSITION_PINS, CACHE_PINS, ATTENTION_PINS, MOTION_PINS, REROTATE_PINS, NOISE_PINS):
         for pin in pins:
             pin()

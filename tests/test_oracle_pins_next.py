@@ -76,6 +76,30 @@ def test_stream_tpos_after_resets_equals_continuous_tpos_minus_shifts():
             assert e[1] == e0[1] - w.chunk_frames * 3 * resets
 
 
+def test_stream_rerotated_keys_keep_scores_continuous():
+    """Right after a reset, the new chunk's queries score the re-rotated window keys as a stream
+    that never resets scores its unrotated keys (fp64 products of the bf16 cache contents; the
+    only difference is bf16 rounding of the rotations)."""
+    w = _small(R=3, W=9)
+    w0 = replace(w, refresh_chunks=0)
+    so, s0 = oracle.StreamOracle(w, 50), oracle.StreamOracle(w0, 50)
+    for c in range(7):                                  # resets at chunks 3 and 6
+        q, k, v = (x[0] for x in qkv_chunk_bits(w, 1, c))
+        so.refresh_rerotate(c)
+        qr = so.append_chunk(c, q, k, v)
+        qr0 = s0.append_chunk(c, q, k, v)
+    nwin = sum(1 for e in so.cache.entries[w.sink_frames:] if e[0] < 6 * w.chunk_frames) * w.hw
+    assert nwin > 0
+    worst = 0.0
+    for h in range(w.heads):
+        qa = bf16_bits_to_f32(qr[:, h, :]).astype(np.float64)
+        qb = bf16_bits_to_f32(qr0[:, h, :]).astype(np.float64)
+        ka = bf16_bits_to_f32(so.cache.keys(h)[w.sink_frames * w.hw:][:nwin]).astype(np.float64)
+        kb = bf16_bits_to_f32(s0.cache.keys(h)[w0.sink_frames * w0.hw:][:nwin]).astype(np.float64)
+        worst = max(worst, float(np.abs(qa @ ka.T - qb @ kb.T).max()))
+    assert worst < 0.5, worst
+
+
 def test_sink_update_copies_the_last_frames():
     w = _small(R=3, W=9)
     so = oracle.StreamOracle(w, 0)
