@@ -45,11 +45,14 @@ __global__ void __launch_bounds__(256) rerotate_kernel(const __grid_constant__ R
     const int h = blockIdx.y;
     const int lsh = rerotate_lane_shift(p.tvecs);
     const int vec = threadIdx.x & ((1 << lsh) - 1);
-    if (!p.active[b] || vec >= p.tvecs) return;
+    if (!p.active[b]) return;
     const int slot = p.Fs + ws;
     sdv2_slot_meta* m = p.meta + static_cast<int64_t>(b) * p.nslots + slot;
     const int64_t fid = m->frame_id;
     if (fid < 0 || fid >= p.limit[b]) return;
+    // the slot's time index moves even when the time segment is empty (rope_t = 0)
+    if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) m->tpos -= p.shift;   // frame_id, which the others read, stays
+    if (vec >= p.tvecs) return;
     // this thread's rows: tok0 + k * (tokens covered by the block in one pass), k < 4
     const int per_pass = 256 >> lsh;
     const int tok0 = blockIdx.x * per_pass * kRerotRowsPerThread + (threadIdx.x >> lsh);
@@ -74,7 +77,6 @@ __global__ void __launch_bounds__(256) rerotate_kernel(const __grid_constant__ R
             base[static_cast<int64_t>(tok) * 16 + vec] = v[k];
         }
     }
-    if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) m->tpos -= p.shift;   // frame_id, which the others read, stays
 }
 
 // Sink update.  Grid: z = stream * F_s + sink slot, y = head, x covers the slot's HW * 16
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kNoiseThreads) noise_kernel(const __grid_const
 
 cudaError_t launch_rerotate(const RerotateParams& p, cudaStream_t s)
 {
-    if (p.B == 0 || p.W == 0 || p.HW == 0 || p.H == 0 || p.tvecs == 0) return cudaSuccess;
+    if (p.B == 0 || p.W == 0 || p.HW == 0 || p.H == 0) return cudaSuccess;   // an empty time segment still moves tpos
     const int tpb = (256 >> rerotate_lane_shift(p.tvecs)) * kRerotRowsPerThread;   // tokens per block
     const dim3 grid(static_cast<unsigned>((p.HW + tpb - 1) / tpb), static_cast<unsigned>(p.H), static_cast<unsigned>(p.B * p.W));
     rerotate_kernel<<<grid, 256, 0, s>>>(p);

@@ -465,7 +465,7 @@ sdv2_status sdv2_rope_refresh_rerotate(const sdv2_stream_cfg* c, const int64_t* 
         p.limit[b] = chunk_index[b] * c->chunk_frames;
         any = any || p.active[b];
     }
-    if (!any || p.tp == 0) return ok();
+    if (!any) return ok();            // with rope_t = 0 nothing rotates, but the slots' tpos still move
     for (int j = 0; j < p.tp; ++j) cos_sin_f32(-p.shift, j, c->rope_t, c->rope_base, &p.cs[j].x);
     return cuda_status(sdv2::launch_rerotate(p, static_cast<cudaStream_t>(stream)), "rerotate launch");
 }
