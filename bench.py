@@ -218,14 +218,14 @@ def oracle_sample(w, seconds_target, seed=0, max_rows=4096):
     keys = np.ascontiguousarray(np.resize(k[0, :, 0, :], (nkv, D)))
     vals = np.ascontiguousarray(np.resize(q[0, :, 1 % w.heads, :], (nkv, D)))
     qrows = np.ascontiguousarray(q[0, :, 0, :])
-    rows_done, t_total, n = 0, 0.0, 8
+    rows_done, t_total, n = 0, 0.0, min(8, w.nq)
     while t_total < seconds_target and rows_done < max_rows:
         rows = rng.choice(w.nq, size=n, replace=False)
         t0 = time.perf_counter()
         oracle.attention_bf16(qrows, keys, vals, 1.0 / math.sqrt(D), rows=rows)
         t_total += time.perf_counter() - t0
         rows_done += n
-        n = min(n * 2, 512)
+        n = min(n * 2, 512, w.nq)
     flops = 4.0 * D * nkv * rows_done
     return flops, t_total, rows_done, oracle.num_threads()
 
