@@ -125,3 +125,41 @@ def test_cuda_graph_replay_equals_eager():
     g.replay()                              # a second replay (the next denoise step) is idempotent
     torch.cuda.synchronize()
     np.testing.assert_array_equal(bits(graphed.out), bits(eager.out))
+
+
+def test_two_sessions_on_two_streams_equal_serial_runs():
+    """Two independent sessions (different configurations, one of them large enough to use key
+    splits) stepped concurrently on two CUDA streams give, bit for bit, what each gives when run
+    alone: no state is shared between workspaces, caches or launches."""
+    wa = W
+    wb = small_workload(WORKLOADS["wan13b_480p"], heads=2, grid_h=10, grid_w=16)
+    chunks = 8
+    ins_a = [_inputs(c) for c in range(chunks)]
+    ins_b = [tuple(t.cuda() for t in qkv_chunk_host(wb, wb.batch, c, seed_offset=9)) for c in range(chunks)]
+    torch.cuda.synchronize()
+
+    def run(concurrent):
+        sa = torch.cuda.Stream()
+        sb = torch.cuda.Stream() if concurrent else sa
+        a = sd.StreamSession(config(wa), 1, wa.start_frames, "cuda", sa)
+        b = sd.StreamSession(config(wb), 1, wb.start_frames, "cuda", sb)
+        torch.cuda.synchronize()
+        oa, ob = [], []
+        for c in range(chunks):
+            a.layer_step(0, [c] * wa.batch, *ins_a[c], stream=sa)
+            with torch.cuda.stream(sa):
+                oa.append(a.out.clone())
+            b.layer_step(0, [c] * wb.batch, *ins_b[c], stream=sb)
+            with torch.cuda.stream(sb):
+                ob.append(b.out.clone())
+        torch.cuda.synchronize()
+        sd.check_device_error(a.ws)
+        sd.check_device_error(b.ws)
+        return [bits(t) for t in oa], [bits(t) for t in ob], sd.last_kv_splits()
+
+    ca, cb, _ = run(True)
+    sa_, sb_, splits_b = run(False)
+    assert splits_b > 1, "the larger session should use key splits"
+    for c in range(chunks):
+        np.testing.assert_array_equal(ca[c], sa_[c], err_msg="session a, chunk %d" % c)
+        np.testing.assert_array_equal(cb[c], sb_[c], err_msg="session b, chunk %d" % c)
