@@ -332,3 +332,35 @@ def test_motion_exact(B, T, hp, wp, ch):
     np.testing.assert_array_equal(ssd.cpu().numpy().view(np.uint64), ssd_ref)
     m_ref = oracle.motion_rms(ssd_ref, hp * wp * ch).astype(np.float32)
     np.testing.assert_array_equal(m.cpu().numpy(), m_ref)
+
+
+@pytest.mark.parametrize("R", [0, 7])
+def test_append_at_a_very_large_chunk_index(R):
+    """A stream a million chunks in (time indices of several million, cache frame numbers past
+    3e6): q_rot and the slot rows equal the oracle's bit-exact RoPE at the oracle's positions,
+    and the slot metadata names the right frame and time index."""
+    w = small_workload(WORKLOADS["tiny"], batch=2, heads=2, refresh_chunks=R, start_frames=[100000, 7])
+    cfg = config(w)
+    sess = sd.StreamSession(cfg, 1, w.start_frames, "cuda")
+    L = sess.layers[0]
+    c = 1_000_003
+    q, k, v = qkv_chunk_host(w, w.batch, 3)
+    sd.rope_append_kv(cfg, w.start_frames, [c, c], q.cuda(), k.cuda(), v.cuda(), sess.q_rot, L.k, L.v, L.meta,
+                      sess.ws)
+    torch.cuda.synchronize()
+    qg, kg, vg, meta = bits(sess.q_rot), bits(L.k), bits(L.v), L.meta.cpu().numpy()
+    hw = w.hw
+    for b in range(w.batch):
+        t, h, ww, frame = oracle.chunk_positions(w.start_frames[b], c, w.chunk_frames, w.grid_h, w.grid_w, R)
+        rep = lambda a: np.repeat(a, w.heads)
+        qo = oracle.rope_spec(bits(q[b]).reshape(-1, 128), rep(t), rep(h), rep(ww), w.rope_t, w.rope_h, w.rope_w,
+                              w.rope_base).reshape(w.nq, w.heads, 128)
+        ko = oracle.rope_spec(bits(k[b]).reshape(-1, 128), rep(t), rep(h), rep(ww), w.rope_t, w.rope_h, w.rope_w,
+                              w.rope_base).reshape(w.nq, w.heads, 128)
+        np.testing.assert_array_equal(qg[b].transpose(1, 0, 2), qo)
+        for i in range(w.chunk_frames):
+            f = int(frame[i * hw])
+            s = oracle.slot_of_frame(f, w.sink_frames, w.window_frames)
+            assert tuple(meta[b, s]) == (f, int(t[i * hw]))
+            np.testing.assert_array_equal(kg[b][:, s * hw:(s + 1) * hw, :], ko[i * hw:(i + 1) * hw].transpose(1, 0, 2))
+            np.testing.assert_array_equal(vg[b][:, s * hw:(s + 1) * hw, :], bits(v[b])[i * hw:(i + 1) * hw].transpose(1, 0, 2))
