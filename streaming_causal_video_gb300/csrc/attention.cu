@@ -32,10 +32,11 @@
 // order and a commit covers all earlier ones, the arrival of S_t(j) also proves that
 // O_t += P_t(j-1) V(j-1) has finished, so O_t can be rescaled without another barrier.
 //
-// With several key splits, each split publishes its unnormalised rows and (max, sum) to the
-// workspace, stored as [dims/4][row][4] floats so that a warp moves 512 contiguous bytes; the
-// split that finishes last for a query pair (an atomic counter) merges them.  No CTA waits for
-// another.
+// With several key splits, each split takes a ticket when its main loop is done.  All but the
+// last publish their unnormalised rows and (max, sum) to the workspace, stored as
+// [dims/4][row][4] floats so that a warp moves 512 contiguous bytes, and count themselves as
+// published; the last merges them with its own rows, still in tensor memory, after a bounded
+// wait for that count (the splits it waits for are already running their epilogues).
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel records kErrTimeout in
 // the workspace error word, tells the other roles to stop, drains its own copies and MMAs and
@@ -372,6 +373,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
         const int q = q0 + rloc;
         const int64_t item = (static_cast<int64_t>(b) * p.H + h) * p.qpairs + qp;
         if (ok && !mbar_wait_bounded(BAR(B_OFULL + t), 0, tmo, abort_flag)) ok = false;
+        // warp-uniform from here on: the epilogue's tensor-memory loads are warp-collective
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) raise_abort(abort_flag, p.err);
         if (ok) tc_fence_after();
         if (p.splits == 1) {
@@ -399,62 +402,84 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                     p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + q] = (m_run + __log2f(l_run)) * kLn2;
             }
         } else {
-            // Split keys: publish this split's unnormalised rows, then the last split to arrive
-            // for this item merges all of them (no CTA waits for another).
-            // Partial rows are stored as groups of four dims, [split item][HD/4][row][4] floats,
-            // so that the 32 rows of a warp write (and the merge reads) 512 contiguous bytes.
-            const int64_t slot = (item * p.splits + sp) * kAttnRowsPerCta + rloc;
-            if (ok) {
-                float4* po = reinterpret_cast<float4*>(p.part_o) + (item * p.splits + sp) * (HD / 4) * kAttnRowsPerCta + rloc;
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
-                    tmem_ld_x32_sync(tO + c * 32, o);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        __stcg(po + (c * 8 + v) * kAttnRowsPerCta,
-                               make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                           __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
-                }
-                __stcg(reinterpret_cast<float2*>(p.part_ml) + slot, make_float2(m_run, l_run));
-            }
-            __threadfence();
-            named_bar_sync(1, 32 * 4 * NQT);
+            // Split keys.  Each split takes a ticket once its main loop is done; the split with
+            // the last ticket merges.  The others publish their unnormalised rows and (max, sum)
+            // -- stored as [split item][HD/4][row][4] floats, so that a warp writes 512
+            // contiguous bytes -- and then count themselves as published; the merger waits
+            // (bounded) for that count and merges the published rows with its own, which stay in
+            // tensor memory.  Every split the merger waits for has already taken its ticket, so
+            // it is running and only has its stores left.
+            int32_t* tickets = p.counters;
+            int32_t* published = p.counters + static_cast<int64_t>(p.B) * p.H * p.qpairs;
             if (threadIdx.x == 0) {
                 int last = 0;
-                if (!*abort_flag) {
-                    const int prev = atomicAdd(p.counters + item, 1);
-                    last = (prev == p.splits - 1);
-                    if (last) p.counters[item] = 0;          // ready for the next call
-                }
+                if (!*abort_flag) last = (atomicAdd(tickets + item, 1) == p.splits - 1) ? 1 : 0;
                 *last_flag = last;
             }
             named_bar_sync(1, 32 * 4 * NQT);
-            if (*last_flag) {
-                __threadfence();
-                float ms[kMaxKvSplits], ls[kMaxKvSplits];
-                float M = -INFINITY;
+            if (!*last_flag) {
+                if (ok) {
+                    const int64_t slot = (item * p.splits + sp) * kAttnRowsPerCta + rloc;
+                    float4* po = reinterpret_cast<float4*>(p.part_o) + (item * p.splits + sp) * (HD / 4) * kAttnRowsPerCta + rloc;
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld_x32_sync(tO + c * 32, o);
 #pragma unroll
-                for (int s2 = 0; s2 < kMaxKvSplits; ++s2) {
-                    if (s2 < p.splits) {
-                        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) +
-                                                 (item * p.splits + s2) * kAttnRowsPerCta + rloc);
-                        ms[s2] = ml.x;
-                        ls[s2] = ml.y;
-                        M = fmaxf(M, ml.x);
+                        for (int v = 0; v < 8; ++v)
+                            __stcg(po + (c * 8 + v) * kAttnRowsPerCta,
+                                   make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                               __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
                     }
+                    __stcg(reinterpret_cast<float2*>(p.part_ml) + slot, make_float2(m_run, l_run));
                 }
-                float L = 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 < kMaxKvSplits; ++s2)
-                    if (s2 < p.splits) {
-                        ms[s2] = ex2_approx(ms[s2] - M);          // weight of split s2
-                        L += ls[s2] * ms[s2];
+                __threadfence();
+                named_bar_sync(1, 32 * 4 * NQT);
+                if (threadIdx.x == 0 && ok && !*abort_flag) atomicAdd(published + item, 1);
+            } else {
+                if (threadIdx.x == 0) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (*reinterpret_cast<volatile int32_t*>(published + item) < p.splits - 1) {
+                        if (*abort_flag || globaltimer_ns() - t0 > tmo) {
+                            raise_abort(abort_flag, p.err);
+                            break;
+                        }
+                        __nanosleep(64);
                     }
-                const float inv = 1.0f / L;
-                if (q < p.Nq) {
+                    // every other split is done with both counters: ready for the next call
+                    tickets[item] = 0;
+                    published[item] = 0;
+                }
+                named_bar_sync(1, 32 * 4 * NQT);
+                __threadfence();
+                if (ok && !*abort_flag) {
+                    float ms[kMaxKvSplits], ls[kMaxKvSplits];
+                    float M = m_run;
+#pragma unroll
+                    for (int s2 = 0; s2 < kMaxKvSplits; ++s2) {
+                        if (s2 < p.splits && s2 != sp) {
+                            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) +
+                                                     (item * p.splits + s2) * kAttnRowsPerCta + rloc);
+                            ms[s2] = ml.x;
+                            ls[s2] = ml.y;
+                            M = fmaxf(M, ml.x);
+                        }
+                    }
+                    // Sums run over the splits in index order, with this split's own rows at its
+                    // own place, so that the result does not depend on which split merges.
+                    ms[sp & (kMaxKvSplits - 1)] = m_run;
+                    ls[sp & (kMaxKvSplits - 1)] = l_run;
+                    float L = 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 < kMaxKvSplits; ++s2)
+                        if (s2 < p.splits) {
+                            ms[s2] = ex2_approx(ms[s2] - M);      // weight of split s2
+                            L += ls[s2] * ms[s2];
+                        }
+                    const float inv = 1.0f / L;
                     uint16_t* dst = p.out + ((static_cast<int64_t>(b) * p.Nq + q) * p.H + h) * HD;
-                    // 32 dims at a time: the eight float4 loads of one split are issued together.
+                    // 32 dims at a time: this split's own rows from tensor memory, the eight float4
+                    // loads of each other split together
 #pragma unroll 1
                     for (int c = 0; c < HD / 32; ++c) {
                         float4 acc[8];
@@ -462,34 +487,44 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                         for (int v = 0; v < 8; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
                         for (int s2 = 0; s2 < p.splits; ++s2) {
-                            const float4* src = reinterpret_cast<const float4*>(p.part_o) +
-                                                ((item * p.splits + s2) * (HD / 4) + c * 8) * kAttnRowsPerCta + rloc;
                             float4 u[8];
+                            if (s2 == sp) {
+                                uint32_t o[32];
+                                tmem_ld_x32_sync(tO + c * 32, o);
 #pragma unroll
-                            for (int v = 0; v < 8; ++v) u[v] = __ldcg(src + v * kAttnRowsPerCta);
-                            const float wgt = ms[s2 < kMaxKvSplits ? s2 : 0];
+                                for (int v = 0; v < 8; ++v)
+                                    u[v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                                       __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+                            } else {
+                                const float4* src = reinterpret_cast<const float4*>(p.part_o) +
+                                                    ((item * p.splits + s2) * (HD / 4) + c * 8) * kAttnRowsPerCta + rloc;
+#pragma unroll
+                                for (int v = 0; v < 8; ++v) u[v] = __ldcg(src + v * kAttnRowsPerCta);
+                            }
+                            const float wgt = ms[s2 & (kMaxKvSplits - 1)];
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
                                 acc[v].x += u[v].x * wgt; acc[v].y += u[v].y * wgt;
                                 acc[v].z += u[v].z * wgt; acc[v].w += u[v].w * wgt;
                             }
                         }
+                        if (q < p.Nq) {
 #pragma unroll
-                        for (int v = 0; v < 8; v += 2) {
-                            uint4 wv;
-                            wv.x = pack_bf16x2(acc[v].x * inv, acc[v].y * inv);
-                            wv.y = pack_bf16x2(acc[v].z * inv, acc[v].w * inv);
-                            wv.z = pack_bf16x2(acc[v + 1].x * inv, acc[v + 1].y * inv);
-                            wv.w = pack_bf16x2(acc[v + 1].z * inv, acc[v + 1].w * inv);
-                            *reinterpret_cast<uint4*>(dst + c * 32 + v * 4) = wv;
+                            for (int v = 0; v < 8; v += 2) {
+                                uint4 wv;
+                                wv.x = pack_bf16x2(acc[v].x * inv, acc[v].y * inv);
+                                wv.y = pack_bf16x2(acc[v].z * inv, acc[v].w * inv);
+                                wv.z = pack_bf16x2(acc[v + 1].x * inv, acc[v + 1].y * inv);
+                                wv.w = pack_bf16x2(acc[v + 1].z * inv, acc[v + 1].w * inv);
+                                *reinterpret_cast<uint4*>(dst + c * 32 + v * 4) = wv;
+                            }
                         }
                     }
-                    if (p.lse) p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + q] = (M + __log2f(L)) * kLn2;
+                    if (p.lse && q < p.Nq) p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + q] = (M + __log2f(L)) * kLn2;
                 }
             }
         }
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == MMA_WARP) {

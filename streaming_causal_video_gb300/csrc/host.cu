@@ -187,7 +187,7 @@ WsLayout ws_layout(const sdv2_stream_cfg* c)
     L.wtab = off;
     off += round_up(sizeof(float2) * c->grid_w * (c->rope_w / 2), 256);
     L.counters = off;
-    off += round_up(sizeof(int32_t) * items, 256);
+    off += round_up(sizeof(int32_t) * 2 * items, 256);       // tickets, published splits
     L.part_ml = off;
     off += round_up(sizeof(float) * 2 * rows, 256);
     L.part_o = off;

@@ -57,7 +57,7 @@ struct AttnParams {
     uint16_t* out;                          // [B][Nq][H][D] bf16
     float* lse;                             // [B][H][Nq] or null
     uint32_t* err;                          // device error word
-    int32_t* counters;                      // [B*H*qpairs] split arrivals (0 between calls)
+    int32_t* counters;                      // [2][B*H*qpairs] split tickets, published splits (0 between calls)
     float* part_ml;                         // [items*splits][256][2] running max (log2) and sum
     float* part_o;                          // [items*splits][256][128] unnormalised output
     int32_t nkv[kMaxAttnStreams];           // valid rows per stream

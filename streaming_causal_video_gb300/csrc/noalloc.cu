@@ -26,7 +26,7 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB per GPU
 constexpr size_t kNaHeader = 256;                            // error word
 constexpr int64_t kNaMaxItems = 16384;                       // (stream, head, 256 rows) items
 constexpr size_t kNaCounters = kNaHeader;
-constexpr size_t kNaCountersBytes = sizeof(int32_t) * kNaMaxItems;
+constexpr size_t kNaCountersBytes = sizeof(int32_t) * 2 * kNaMaxItems;   // tickets, published splits
 constexpr size_t kNaPartMl = kNaCounters + kNaCountersBytes;
 // Rows of split partials that fit: 8 bytes of (max, sum) + 512 bytes of output per row,
 // rounded down to whole 256-row units.
