@@ -185,7 +185,9 @@ sdv2_status sdv2_qkv_rope_append(const sdv2_stream_cfg* cfg, const int64_t* star
  * Numerics: bf16 tensor-core products with fp32 accumulation, online softmax in fp32.
  * Work split: one CTA per (stream, head, 256 query rows, key split); the key range of an item
  * is cut into 1-4 splits chosen to fill whole waves of the GPU's SMs; the split that finishes
- * last merges the others' partial rows (log-sum-exp weights) and writes the output.
+ * its keys last merges the others' partial rows with its own (log-sum-exp weights, splits
+ * summed in index order, so the output does not depend on which split merges) and writes the
+ * output.  The result is deterministic: the same inputs give the same bits on every call.
  * Limits: B <= 16; the device must be sm_103 (tcgen05 tensor cores).
  */
 sdv2_status sdv2_chunk_attention(const sdv2_stream_cfg* cfg, const int64_t* chunk_index,
