@@ -163,7 +163,7 @@ sdv2_status sdv2_rope_append_kv(const sdv2_stream_cfg* cfg, const int64_t* start
  * Numerics: bf16 products with fp32 accumulation (tcgen05 tensor cores), + bias in fp32, q/k
  * pairs rotated in fp32 as (fmaf(x, c, -(y*s)), fmaf(x, s, y*c)), one bf16 RNE per output.
  * (It differs from projecting to bf16 first and calling sdv2_rope_append_kv by that one
- * rounding.)  Limits: H even; the limits of sdv2_rope_append_kv.
+ * rounding.)  Limits: those of sdv2_rope_append_kv.
  */
 sdv2_status sdv2_qkv_rope_append(const sdv2_stream_cfg* cfg, const int64_t* start_frame,
                                  const int64_t* chunk_index, const void* x, int64_t x_token_stride,

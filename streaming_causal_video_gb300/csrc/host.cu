@@ -398,7 +398,6 @@ sdv2_status sdv2_qkv_rope_append(const sdv2_stream_cfg* c, const int64_t* start_
         if (!p || !aligned16(p)) return fail(SDV2_ERR_INVALID_ARG, "device pointers must be non-null and 16-byte aligned");
     if (bias && (reinterpret_cast<uintptr_t>(bias) & 15u)) return fail(SDV2_ERR_INVALID_ARG, "bias must be 16-byte aligned");
     const int64_t C = static_cast<int64_t>(c->heads) * c->head_dim;
-    if (c->heads % 2) return fail(SDV2_ERR_UNSUPPORTED, "the fused projection needs an even number of heads");
     const int64_t ld = x_token_stride ? x_token_stride : C;
     if (ld < C || (ld % 8)) return fail(SDV2_ERR_INVALID_ARG, "x_token_stride must be >= H*D and a multiple of 8");
     const int64_t M = static_cast<int64_t>(c->batch) * hw_of(c) * c->chunk_frames;

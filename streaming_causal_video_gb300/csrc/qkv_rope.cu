@@ -9,13 +9,16 @@
 // frame and chunk, as in sdv2_rope_append_kv) and writes q_rot (head-major) and k_rot, v into
 // the frames' cache slots, without a round trip of q, k, v through memory.
 //
-// Tiling: a CTA computes 128 tokens x 256 features (two heads of one of q, k, v) over the whole
-// hidden dimension in steps of 64 (128-byte swizzled TMA boxes), through a 2-stage ring
-// (48 KB per stage), so that two CTAs share an SM and one's epilogue overlaps the other's main
-// loop.  The accumulator (128 lanes x 256 fp32 columns) lives in tensor memory.
+// Tiling: a CTA computes 256 tokens x 192 features as two 128-row halves, each with its own
+// fp32 accumulator in tensor memory (columns 0 and 256), over the whole hidden dimension in
+// steps of 64 (128-byte swizzled TMA boxes) through a 3-stage ring of 56 KB stages; both halves
+// multiply the same weight stage, so a stage carries 22 % fewer bytes per flop than a 128 x 256
+// tile.  One CTA per SM; 456 tiles at the Wan-1.3B 480p shape, three full waves.  A tile may
+// straddle heads and the q|k|v boundaries: the epilogue finds the type and head of each
+// 32-feature chunk.
 //   warp 0: TMA producer; warp 1: MMA issuer (converged: every lane polls the stage barrier and
-//   a warp vote agrees on the outcome; elect.sync issues); warps 2-5: epilogue,
-//   thread = token row = TMEM lane.
+//   a warp vote agrees on the outcome; elect.sync issues); warps 2-9: epilogue, two per TMEM lane
+//   quarter (one per half), thread = token row.
 // Rounding: acc (fp32, fp32 accumulation) + bias (fp32 add); q and k pairs rotated in fp32 as
 // (fmaf(x, c, -(y*s)), fmaf(x, s, y*c)); one bf16 round-to-nearest-even per output.
 #include <cuda_bf16.h>
@@ -29,16 +32,19 @@
 namespace sdv2 {
 namespace {
 
-constexpr int QBM = 128;                       // tokens per tile
-constexpr int QBN = 256;                       // features per tile
+constexpr int QBM = 256;                       // tokens per tile: two halves of 128 rows
+constexpr int QBN = 192;                       // features per tile
 constexpr int QBK = 64;                        // hidden elements per step (128 bytes of bf16)
-constexpr int QST = 2;                         // ring stages
-constexpr uint32_t A_BYTES = QBM * QBK * 2;    // 16 KB
-constexpr uint32_t B_BYTES = QBN * QBK * 2;    // 32 KB
+constexpr int QST = 3;                         // ring stages
+constexpr uint32_t A_BYTES = QBM * QBK * 2;    // 32 KB
+constexpr uint32_t A_HALF = A_BYTES / 2;       // rows 128..255 of the A box start here
+constexpr uint32_t B_BYTES = QBN * QBK * 2;    // 24 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int QTHREADS = 6 * 32;
-constexpr uint32_t QTMEM_COLS = 256;
+constexpr int QTHREADS = 10 * 32;
+constexpr uint32_t QTMEM_COLS = 512;           // accumulators at columns 0 and 256
 constexpr uint32_t QSMEM_BYTES = QST * STAGE_BYTES + 256 + 1024;
+static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "128-byte swizzle needs 1024-byte aligned tiles");
+static_assert(QSMEM_BYTES <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
@@ -111,10 +117,11 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_bf16_f32(QBM, QBN, false);
+        constexpr uint32_t idesc = idesc_bf16_f32(128, QBN, false);
         const uint64_t dA = sdesc_sw128(s0, 16, 1024);
         const uint64_t dB = sdesc_sw128(s0 + A_BYTES, 16, 1024);
         constexpr uint64_t kStage = STAGE_BYTES >> 4;
+        constexpr uint64_t kHalf = A_HALF >> 4;
         bool ok = true;
         for (int kk = 0; kk < ksteps; ++kk) {
             const int st = kk % QST;
@@ -126,10 +133,14 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
             tc_fence_after();
             const uint64_t a = dA + static_cast<uint64_t>(st) * kStage;
             const uint64_t b = dB + static_cast<uint64_t>(st) * kStage;
+            // both halves of the tile multiply the same weight stage
 #pragma unroll
-            for (int k = 0; k < QBK / 16; ++k)
-                mma_ss_warp(tmem, a + static_cast<uint64_t>(k * 2), b + static_cast<uint64_t>(k * 2), idesc,
-                            (kk > 0 || k > 0) ? 1u : 0u);
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int k = 0; k < QBK / 16; ++k)
+                    mma_ss_warp(tmem + static_cast<uint32_t>(hh * 256), a + static_cast<uint64_t>(hh) * kHalf +
+                                static_cast<uint64_t>(k * 2), b + static_cast<uint64_t>(k * 2), idesc,
+                                (kk > 0 || k > 0) ? 1u : 0u);
             mma_commit_warp(QBAR(QST + st));
         }
         if (!ok && lane == 0) {
@@ -144,12 +155,16 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ epilogue: 128 threads
+        // ------------------------------------------------------------ epilogue: 256 threads
+        // warps 2-5 read the accumulator of rows 0..127, warps 6-9 that of rows 128..255; a warp
+        // reaches the TMEM lanes of its quarter (warp index mod 4)
+        const int hh = (warp - 2) >> 2;
         const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
-        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const int row = hh * 128 + quarter * 32 + lane;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(hh * 256);
         bool ok = mbar_wait_bounded(QBAR(2 * QST), 0, tmo, abort_flag) && !*abort_flag;
-        if (!ok && row == 0) atomicOr(p.err, kErrTimeout);
+        ok = __all_sync(0xffffffffu, ok);               // the TMEM loads below are warp-collective
+        if (!ok && lane == 0) atomicOr(p.err, kErrTimeout);
         tc_fence_after();
         const int m = m0 + row;
         const bool valid = ok && m < p.M;
@@ -162,57 +177,54 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
         const int gw = r - gh * p.grid_w;
         const FrameDesc fd = p.frames[b * p.F + i];
         const int hd = p.H * 128;
-        const int type = n0 / hd;                      // 0 = q, 1 = k, 2 = v
-        const int head0 = (n0 - type * hd) / 128;
         const int64_t rows = static_cast<int64_t>(p.nslots) * p.HW;
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-            const int head = head0 + hh;
+        for (int cchunk = 0; cchunk < QBN / 32; ++cchunk) {
+            uint32_t a[32];
+            tmem_ld_x32_sync(trow + static_cast<uint32_t>(cchunk * 32), a);
+            if (!valid) continue;
+            const int f0 = n0 + cchunk * 32;              // feature of a[0]
+            const int type = f0 / hd;                     // 0 = q, 1 = k, 2 = v
+            const int fl = f0 - type * hd;
+            const int head = fl >> 7;
+            const int d0 = fl & 127;                      // first dim of the chunk in its head
             const int64_t bh = static_cast<int64_t>(b) * p.H + head;
-            uint16_t* dst = (type == 0) ? p.q_rot + (bh * p.Nq + n) * 128
-                          : (type == 1) ? p.k_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128
-                                        : p.v_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128;
-#pragma unroll 1
-            for (int cchunk = 0; cchunk < 4; ++cchunk) {
-                uint32_t a[32];
-                tmem_ld_x32_sync(trow + static_cast<uint32_t>(hh * 128 + cchunk * 32), a);
-                if (!valid) continue;
-                const int f0 = n0 + hh * 128 + cchunk * 32;   // feature of a[0]
-                uint32_t o[16];
+            uint16_t* dst = (type == 0) ? p.q_rot + (bh * p.Nq + n) * 128 + d0
+                          : (type == 1) ? p.k_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0
+                                        : p.v_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0;
+            uint32_t o[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    float x = __uint_as_float(a[2 * u]);
-                    float y = __uint_as_float(a[2 * u + 1]);
-                    if (p.bias) {
-                        x = __fadd_rn(x, p.bias[f0 + 2 * u]);
-                        y = __fadd_rn(y, p.bias[f0 + 2 * u + 1]);
-                    }
-                    if (type < 2) {
-                        const int pr = cchunk * 16 + u;       // rotation pair inside the head
-                        float2 cs;
-                        if (pr < p.tp) cs = p.tcs[(b * p.F + i) * p.tp + pr];
-                        else if (pr < p.tp + p.hp) cs = p.h_tab[gh * p.hp + (pr - p.tp)];
-                        else cs = p.w_tab[gw * p.wp + (pr - p.tp - p.hp)];
-                        const float xr = __fmaf_rn(x, cs.x, -__fmul_rn(y, cs.y));
-                        const float yr = __fmaf_rn(x, cs.y, __fmul_rn(y, cs.x));
-                        x = xr;
-                        y = yr;
-                    }
-                    o[u] = pack2(x, y);
+            for (int u = 0; u < 16; ++u) {
+                float x = __uint_as_float(a[2 * u]);
+                float y = __uint_as_float(a[2 * u + 1]);
+                if (p.bias) {
+                    x = __fadd_rn(x, p.bias[f0 + 2 * u]);
+                    y = __fadd_rn(y, p.bias[f0 + 2 * u + 1]);
                 }
-                uint4* d4 = reinterpret_cast<uint4*>(dst + cchunk * 32);
+                if (type < 2) {
+                    const int pr = (d0 >> 1) + u;             // rotation pair inside the head
+                    float2 cs;
+                    if (pr < p.tp) cs = p.tcs[(b * p.F + i) * p.tp + pr];
+                    else if (pr < p.tp + p.hp) cs = p.h_tab[gh * p.hp + (pr - p.tp)];
+                    else cs = p.w_tab[gw * p.wp + (pr - p.tp - p.hp)];
+                    const float xr = __fmaf_rn(x, cs.x, -__fmul_rn(y, cs.y));
+                    const float yr = __fmaf_rn(x, cs.y, __fmul_rn(y, cs.x));
+                    x = xr;
+                    y = yr;
+                }
+                o[u] = pack2(x, y);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            if (type == 1 && head == 0 && d0 == 0 && r == 0) {    // one writer per (stream, frame)
+                sdv2_slot_meta md;
+                md.frame_id = fd.frame;
+                md.tpos = fd.tpos;
+                p.meta[static_cast<int64_t>(b) * p.nslots + fd.slot] = md;
             }
         }
-        if (valid && type == 1 && head0 == 0 && r == 0) {
-            sdv2_slot_meta md;
-            md.frame_id = fd.frame;
-            md.tpos = fd.tpos;
-            p.meta[static_cast<int64_t>(b) * p.nslots + fd.slot] = md;
-        }
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -1,5 +1,5 @@
 """Seeded sweep of the fused QKV projection + Causal-RoPE + append against the fp64 oracle:
-random even head counts, grids (ragged 128-token tiles), chunk sizes, stream counts, RoPE splits,
+random head counts (odd and even), grids (ragged 256-token tiles), chunk sizes, stream counts, RoPE splits,
 refresh periods, with and without bias, and padded input token strides.  Each chunk: q_rot, the
 appended k and v rows within 2^-8 of each rotation pair's norm, slot metadata exact.
 SDV2_SWEEP_QKV_CONFIGS sets the number of configurations (default 6)."""
@@ -40,7 +40,7 @@ def _random_case(seed):
     big = seed % 3 == 2
     gh = int(rng.integers(8, 20)) if big else int(rng.integers(1, 9))
     gw = int(rng.integers(8, 24)) if big else int(rng.integers(1, 11))
-    w = small_workload(WORKLOADS["tiny"], batch=B, heads=int(rng.choice([2, 4, 6])), grid_h=gh, grid_w=gw,
+    w = small_workload(WORKLOADS["tiny"], batch=B, heads=int(rng.choice([1, 2, 3, 4, 5, 6])), grid_h=gh, grid_w=gw,
                        chunk_frames=F, sink_frames=Fs, window_frames=W, refresh_chunks=int(rng.choice([0, 2, 3])),
                        rope_t=rt, rope_h=rh, rope_w=128 - rt - rh,
                        start_frames=[int(x) for x in rng.integers(0, 120000, B)])
