@@ -3,7 +3,7 @@
 For each HBM-bound call: algorithmic bytes per call, mean time over repeated calls on buffers
 larger than L2 (several distinct layer caches are cycled), achieved GB/s and the fraction of
 the copy-bandwidth peak.  For attention: flops per call and TFLOP/s.  Prints one JSON line per
-measurement.  Run: python -m streaming_causal_video_gb300.kernel_timings [--peak-gbs X]
+measurement.  Run: python -m streaming_causal_video_gb300.kernel_timings [--peak-gbs X] [--only qkv,...]
 """
 import argparse
 import json
@@ -39,7 +39,13 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--peak-gbs", type=float, default=0.0, help="HBM peak (GB/s); default: MEASURED_PEAKS.json or 6800")
     ap.add_argument("--layers", type=int, default=8, help="distinct layer caches cycled (more than L2 in total)")
+    ap.add_argument("--only", default="", help="comma-separated subset of: append, attention, rerotate, sink, "
+                    "qkv, unfused, motion, noise (default: all)")
     args = ap.parse_args()
+    only = {x.strip() for x in args.only.split(",") if x.strip()}
+
+    def want(k):
+        return not only or k in only
     peak = args.peak_gbs
     src = "given"
     if not peak:
@@ -87,14 +93,16 @@ def main():
         l = i % nl
         L = sess.layers[l]
         sd.rope_append_kv(cfg, w.start_frames, [steady], *qkv[l], sess.q_rot, L.k, L.v, L.meta, sess.ws, stream)
-    report("sdv2_rope_append_kv", w.name, bytes_per_call=w.nq * w.heads * 1536, ms=_time(rope, 60, stream))
+    if want("append"):
+        report("sdv2_rope_append_kv", w.name, bytes_per_call=w.nq * w.heads * 1536, ms=_time(rope, 60, stream))
 
     def attn(i):
         L = sess.layers[i % nl]
         sd.chunk_attention(cfg, [steady], sess.q_rot, L.k, L.v, sess.out, sess.ws, stream=stream)
     nkv = sd.visible_tokens(cfg, steady)
-    report("sdv2_chunk_attention", w.name, flops_per_call=4.0 * w.heads * 128 * w.nq * nkv, ms=_time(attn, 30, stream),
-           extra={"kv_splits": sd.last_kv_splits()})
+    if want("attention"):
+        report("sdv2_chunk_attention", w.name, flops_per_call=4.0 * w.heads * 128 * w.nq * nkv,
+               ms=_time(attn, 30, stream), extra={"kv_splits": sd.last_kv_splits()})
 
     # re-rotation at a refresh chunk: every window slot holds an earlier frame (R = 7 chunks so
     # that chunk 7 is a refresh chunk); time-axis vectors of the window keys are read and written
@@ -106,15 +114,17 @@ def main():
     def rerot(i):
         L = sess.layers[i % nl]
         sd.rope_refresh_rerotate(cfg_r, [7], L.k, L.meta, stream)
-    report("sdv2_rope_refresh_rerotate", w.name + " (window of 18 frames)", bytes_per_call=rr_bytes,
-           ms=_time(rerot, 60, stream))
+    if want("rerotate"):
+        report("sdv2_rope_refresh_rerotate", w.name + " (window of 18 frames)", bytes_per_call=rr_bytes,
+               ms=_time(rerot, 60, stream))
 
     sink_bytes = w.sink_frames * w.hw * w.heads * 256 * 2 * 2
 
     def sink(i):
         L = sess.layers[i % nl]
         sd.sink_update(cfg, [steady], [1], L.k, L.v, L.meta, stream)
-    report("sdv2_sink_update", w.name + " (3 sink frames)", bytes_per_call=sink_bytes, ms=_time(sink, 60, stream))
+    if want("sink"):
+        report("sdv2_sink_update", w.name + " (3 sink frames)", bytes_per_call=sink_bytes, ms=_time(sink, 60, stream))
     # fused QKV projection + RoPE + append vs the unfused sequence (projection GEMM through
     # torch/cuBLAS to bf16, then sdv2_rope_append_kv)
     C = w.heads * w.head_dim
@@ -127,10 +137,10 @@ def main():
         L = sess.layers[i % nl]
         sd.qkv_rope_append(cfg, w.start_frames, [steady], xs[i % nl], Wq, sess.q_rot, L.k, L.v, L.meta, sess.ws,
                            bias=bq, stream=stream)
-    ms_f = _time(fused, 60, stream)
-    report("sdv2_qkv_rope_append", w.name + " (x [4680][1536] @ W[4608][1536]^T + bias, RoPE, append)",
-           flops_per_call=gemm_flops, ms=ms_f,
-           extra={"bytes_min": int((w.nq * C + 3 * C * C) * 2 + w.nq * 3 * C * 2)})
+    if want("qkv"):
+        report("sdv2_qkv_rope_append", w.name + " (x [4680][1536] @ W[4608][1536]^T + bias, RoPE, append)",
+               flops_per_call=gemm_flops, ms=_time(fused, 60, stream),
+               extra={"bytes_min": int((w.nq * C + 3 * C * C) * 2 + w.nq * 3 * C * 2)})
     ybuf = torch.empty((1, w.nq, 3 * C), dtype=torch.bfloat16, device=dev)
 
     def unfused(i):
@@ -142,10 +152,13 @@ def main():
         cfg_s = sd.StreamConfig.make(**stream_config_dict(w, qkv_token_stride=3 * C))
         sd.rope_append_kv(cfg_s, w.start_frames, [steady], y[:, :, 0], y[:, :, 1], y[:, :, 2], sess.q_rot, L.k, L.v,
                           L.meta, sess.ws, stream)
-    ms_u = _time(unfused, 60, stream)
-    report("unfused: torch.matmul (cuBLAS) + bias + sdv2_rope_append_kv", w.name, flops_per_call=gemm_flops, ms=ms_u)
+    if want("unfused"):
+        report("unfused: torch.matmul (cuBLAS) + bias + sdv2_rope_append_kv", w.name, flops_per_call=gemm_flops,
+               ms=_time(unfused, 60, stream))
     del sess, qkv
     torch.cuda.empty_cache()
+    if not (want("motion") or want("noise")):
+        return out
 
     # ---- stream batch: motion over 4 x 501 frames of 480x832x3, then the noise controller
     wb = WORKLOADS["stream_batch"]
@@ -156,14 +169,16 @@ def main():
 
     def motion(i):
         sd.motion_l2(frames, ssd, m, stream)
-    report("sdv2_motion_l2", "stream_batch: 4 x 501 frames of 480x832x3", bytes_per_call=frames.numel(),
-           ms=_time(motion, 10, stream))
+    if want("motion"):
+        report("sdv2_motion_l2", "stream_batch: 4 x 501 frames of 480x832x3", bytes_per_call=frames.numel(),
+               ms=_time(motion, 10, stream))
     ctl = sd.NoiseCtl(motion_lo=2.0, motion_hi=12.0, rate_lo=0.1, rate_hi=0.9, ema=0.5, more_noise_when_fast=1)
     rate = torch.empty_like(m)
 
     def noise(i):
         sd.noise_from_motion(ctl, m, rate, None, stream)
-    report("sdv2_noise_from_motion", "stream_batch: 4 x 500 motion values", ms=_time(noise, 100, stream))
+    if want("noise"):
+        report("sdv2_noise_from_motion", "stream_batch: 4 x 500 motion values", ms=_time(noise, 100, stream))
     return out
 
 
