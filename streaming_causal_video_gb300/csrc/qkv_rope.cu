@@ -18,7 +18,8 @@
 // 32-feature chunk.
 //   warp 0: TMA producer; warp 1: MMA issuer (converged: every lane polls the stage barrier and
 //   a warp vote agrees on the outcome; elect.sync issues); warps 2-9: epilogue, two per TMEM lane
-//   quarter (one per half), thread = token row.
+//   quarter (one per half), thread = token row, with the next 32-column TMEM load in flight while
+//   the current chunk is rotated and stored (bias read as float4).
 // Rounding: acc (fp32, fp32 accumulation) + bias (fp32 add); q and k pairs rotated in fp32 as
 // (fmaf(x, c, -(y*s)), fmaf(x, s, y*c)); one bf16 round-to-nearest-even per output.
 #include <cuda_bf16.h>
@@ -50,6 +51,26 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Starts a load of 32 consecutive 32-bit columns of this thread's TMEM lane; the registers hold
+// the values only after tmem_wait_ld_tied on the same array.
+__device__ __forceinline__ void tmem_ld_x32_async(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+// Waits for this thread's TMEM loads.  The array is an in-out operand, so no use of it is
+// scheduled above the wait and its registers stay reserved while the load is in flight.
+__device__ __forceinline__ void tmem_wait_ld_tied(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
 }
 
 __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constant__ QkvRopeParams p)
@@ -178,51 +199,71 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
         const FrameDesc fd = p.frames[b * p.F + i];
         const int hd = p.H * 128;
         const int64_t rows = static_cast<int64_t>(p.nslots) * p.HW;
-#pragma unroll 1
+        const float2* t_row = p.tcs + (b * p.F + i) * p.tp;
+        const float2* h_row = p.h_tab + gh * p.hp;
+        const float2* w_row = p.w_tab + gw * p.wp;
+        // the next chunk's TMEM load is in flight while this chunk is rotated and stored
+        uint32_t a[2][32];
+        tmem_ld_x32_async(trow, a[0]);
+        tmem_wait_ld_tied(a[0]);
+#pragma unroll
         for (int cchunk = 0; cchunk < QBN / 32; ++cchunk) {
-            uint32_t a[32];
-            tmem_ld_x32_sync(trow + static_cast<uint32_t>(cchunk * 32), a);
-            if (!valid) continue;
-            const int f0 = n0 + cchunk * 32;              // feature of a[0]
-            const int type = f0 / hd;                     // 0 = q, 1 = k, 2 = v
-            const int fl = f0 - type * hd;
-            const int head = fl >> 7;
-            const int d0 = fl & 127;                      // first dim of the chunk in its head
-            const int64_t bh = static_cast<int64_t>(b) * p.H + head;
-            uint16_t* dst = (type == 0) ? p.q_rot + (bh * p.Nq + n) * 128 + d0
-                          : (type == 1) ? p.k_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0
-                                        : p.v_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0;
-            uint32_t o[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                float x = __uint_as_float(a[2 * u]);
-                float y = __uint_as_float(a[2 * u + 1]);
+            uint32_t(&cur)[32] = a[cchunk & 1];
+            if (cchunk + 1 < QBN / 32)
+                tmem_ld_x32_async(trow + static_cast<uint32_t>((cchunk + 1) * 32), a[(cchunk + 1) & 1]);
+            if (valid) {
+                const int f0 = n0 + cchunk * 32;              // feature of cur[0]
+                const int type = f0 / hd;                     // 0 = q, 1 = k, 2 = v
+                const int fl = f0 - type * hd;
+                const int head = fl >> 7;
+                const int d0 = fl & 127;                      // first dim of the chunk in its head
+                const int64_t bh = static_cast<int64_t>(b) * p.H + head;
+                uint16_t* dst = (type == 0) ? p.q_rot + (bh * p.Nq + n) * 128 + d0
+                              : (type == 1) ? p.k_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0
+                                            : p.v_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0;
+                float bv[32];
                 if (p.bias) {
-                    x = __fadd_rn(x, p.bias[f0 + 2 * u]);
-                    y = __fadd_rn(y, p.bias[f0 + 2 * u + 1]);
-                }
-                if (type < 2) {
-                    const int pr = (d0 >> 1) + u;             // rotation pair inside the head
-                    float2 cs;
-                    if (pr < p.tp) cs = p.tcs[(b * p.F + i) * p.tp + pr];
-                    else if (pr < p.tp + p.hp) cs = p.h_tab[gh * p.hp + (pr - p.tp)];
-                    else cs = p.w_tab[gw * p.wp + (pr - p.tp - p.hp)];
-                    const float xr = __fmaf_rn(x, cs.x, -__fmul_rn(y, cs.y));
-                    const float yr = __fmaf_rn(x, cs.y, __fmul_rn(y, cs.x));
-                    x = xr;
-                    y = yr;
-                }
-                o[u] = pack2(x, y);
-            }
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
+                    const float4* b4 = reinterpret_cast<const float4*>(p.bias + f0);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-            if (type == 1 && head == 0 && d0 == 0 && r == 0) {    // one writer per (stream, frame)
-                sdv2_slot_meta md;
-                md.frame_id = fd.frame;
-                md.tpos = fd.tpos;
-                p.meta[static_cast<int64_t>(b) * p.nslots + fd.slot] = md;
+                    for (int v = 0; v < 8; ++v) {
+                        const float4 t4 = b4[v];
+                        bv[4 * v] = t4.x;
+                        bv[4 * v + 1] = t4.y;
+                        bv[4 * v + 2] = t4.z;
+                        bv[4 * v + 3] = t4.w;
+                    }
+                }
+                uint32_t o[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    float x = __uint_as_float(cur[2 * u]);
+                    float y = __uint_as_float(cur[2 * u + 1]);
+                    if (p.bias) {
+                        x = __fadd_rn(x, bv[2 * u]);
+                        y = __fadd_rn(y, bv[2 * u + 1]);
+                    }
+                    if (type < 2) {
+                        const int pr = (d0 >> 1) + u;             // rotation pair inside the head
+                        const float2 cs = pr < p.tp ? t_row[pr]
+                                        : pr < p.tp + p.hp ? h_row[pr - p.tp] : w_row[pr - p.tp - p.hp];
+                        const float xr = __fmaf_rn(x, cs.x, -__fmul_rn(y, cs.y));
+                        const float yr = __fmaf_rn(x, cs.y, __fmul_rn(y, cs.x));
+                        x = xr;
+                        y = yr;
+                    }
+                    o[u] = pack2(x, y);
+                }
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+                if (type == 1 && head == 0 && d0 == 0 && r == 0) {    // one writer per (stream, frame)
+                    sdv2_slot_meta md;
+                    md.frame_id = fd.frame;
+                    md.tpos = fd.tpos;
+                    p.meta[static_cast<int64_t>(b) * p.nslots + fd.slot] = md;
+                }
             }
+            if (cchunk + 1 < QBN / 32) tmem_wait_ld_tied(a[(cchunk + 1) & 1]);
         }
     }
     tc_fence_before();
