@@ -140,6 +140,10 @@ def _fused_reference(w, start, c, x_b, W, bias):
 
 @pytest.mark.parametrize("name,over,chunks,attend", [
     ("tiny", dict(heads=2, window_frames=4, refresh_chunks=3, batch=2, start_frames=[0, 500]), 7, True),
+    # odd head count: 192-feature tiles straddle heads and the q|k|v boundaries; 405 tokens per
+    # stream leave a ragged 256-token tile
+    ("tiny", dict(heads=3, grid_h=9, grid_w=15, window_frames=5, refresh_chunks=2, batch=2,
+                  start_frames=[7, 90000]), 4, True),
     ("wan13b_480p", dict(), 2, False),
 ])
 def test_fused_qkv_rope_append_matches_fp64(name, over, chunks, attend):
@@ -185,3 +189,42 @@ def test_fused_qkv_rope_append_matches_fp64(name, over, chunks, attend):
                     ref, _ = oracle.attention_f64(refs[b][:, hh, :], K, V, 1 / math.sqrt(w.head_dim))
                     err = np.abs(out[b, :, hh, :] - ref)
                     assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (c, b, hh, err.max(), err.mean())
+
+
+def test_fused_qkv_rope_append_at_14b_shape_sampled_rows():
+    """Wan-14B 480p shape (40 heads, C = 5120, 80 feature tiles of 192, 19 token tiles of 256):
+    sampled token rows of q_rot, k and v against the fp64 projection + RoPE of those rows."""
+    w = WORKLOADS["wan14b_480p"]
+    cfg = config(w)
+    starts = list(w.start_frames)
+    sess = sd.StreamSession(cfg, 1, starts, "cuda")
+    L = sess.layers[0]
+    C = w.heads * w.head_dim
+    c = 9                                           # window already wrapped: slots != frames
+    x, W, bias = _proj_inputs(w, c, seed=3)
+    sd.qkv_rope_append(cfg, starts, [c], x.cuda(), W.cuda(), sess.q_rot, L.k, L.v, L.meta, sess.ws,
+                       bias=bias.cuda())
+    torch.cuda.synchronize()
+    sd.check_device_error(sess.ws)
+    rows = np.unique(np.concatenate([np.arange(0, 4), np.linspace(0, w.nq - 1, 60).astype(np.int64),
+                                     np.arange(w.nq - 4, w.nq), np.arange(255, 258), np.arange(1559, 1562)]))
+    y = oracle.qkv_project(bits(x[0][torch.from_numpy(rows)].contiguous()), bits(W), bias.numpy())
+    t, h, ww, frame = oracle.chunk_positions(starts[0], c, w.chunk_frames, w.grid_h, w.grid_w, w.refresh_chunks)
+    rep = lambda a: np.repeat(a[rows].astype(np.float64), w.heads)
+    rot = lambda z: oracle.rope_ideal(z.reshape(-1, w.head_dim), rep(t), rep(h), rep(ww), w.rope_t, w.rope_h,
+                                      w.rope_w, w.rope_base).reshape(len(rows), w.heads, w.head_dim)
+    q, k = rot(y[:, :C]), rot(y[:, C:2 * C])
+    v = y[:, 2 * C:].reshape(len(rows), w.heads, w.head_dim)
+    qg = to_f64(sess.q_rot[0][:, torch.from_numpy(rows).cuda()])            # [H][rows][D]
+    _close(qg.transpose(1, 0, 2), q, "q_rot")
+    hw = w.hw
+    meta = L.meta.cpu().numpy()[0]
+    slot_rows = []
+    for n in rows:
+        f = c * w.chunk_frames + int(n) // hw
+        s = oracle.slot_of_frame(f, w.sink_frames, w.window_frames)
+        assert tuple(meta[s]) == (f, int(t[(int(n) // hw) * hw])), (n, s, tuple(meta[s]))
+        slot_rows.append(s * hw + int(n) % hw)
+    idx = torch.tensor(slot_rows, device="cuda")
+    _close(to_f64(L.k[0][:, idx]).transpose(1, 0, 2), k, "k rows")
+    _close(to_f64(L.v[0][:, idx]).transpose(1, 0, 2), v, "v rows")
