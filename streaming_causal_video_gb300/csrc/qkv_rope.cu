@@ -19,7 +19,10 @@
 //   warp 0: TMA producer; warp 1: MMA issuer (converged: every lane polls the stage barrier and
 //   a warp vote agrees on the outcome; elect.sync issues); warps 2-9: epilogue, two per TMEM lane
 //   quarter (one per half), thread = token row, with the next 32-column TMEM load in flight while
-//   the current chunk is rotated and stored (bias read as float4).
+//   the current chunk is rotated and stored (bias read as float4).  A chunk's 16 cos/sin pairs
+//   are loaded into registers before any is used: each pair's table (time, h or w axis) is
+//   picked by a pointer select, so the 16 loads issue back to back instead of one per branch
+//   of the axis test (that had left the epilogue longer than the main loop).
 // Rounding: acc (fp32, fp32 accumulation) + bias (fp32 add); q and k pairs rotated in fp32 as
 // (fmaf(x, c, -(y*s)), fmaf(x, s, y*c)); one bf16 round-to-nearest-even per output.
 #include <cuda_bf16.h>
@@ -233,6 +236,16 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
                         bv[4 * v + 3] = t4.w;
                     }
                 }
+                float2 csv[16];
+                if (type < 2) {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int pr = (d0 >> 1) + u;
+                        const float2* src = pr < p.tp ? t_row + pr
+                                          : pr < p.tp + p.hp ? h_row + (pr - p.tp) : w_row + (pr - p.tp - p.hp);
+                        csv[u] = *src;           // generic load: t pairs live in the launch parameters
+                    }
+                }
                 uint32_t o[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
@@ -243,9 +256,7 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
                         y = __fadd_rn(y, bv[2 * u + 1]);
                     }
                     if (type < 2) {
-                        const int pr = (d0 >> 1) + u;             // rotation pair inside the head
-                        const float2 cs = pr < p.tp ? t_row[pr]
-                                        : pr < p.tp + p.hp ? h_row[pr - p.tp] : w_row[pr - p.tp - p.hp];
+                        const float2 cs = csv[u];
                         const float xr = __fmaf_rn(x, cs.x, -__fmul_rn(y, cs.y));
                         const float yr = __fmaf_rn(x, cs.y, __fmul_rn(y, cs.x));
                         x = xr;

@@ -40,7 +40,7 @@ def main():
     ap.add_argument("--peak-gbs", type=float, default=0.0, help="HBM peak (GB/s); default: MEASURED_PEAKS.json or 6800")
     ap.add_argument("--layers", type=int, default=8, help="distinct layer caches cycled (more than L2 in total)")
     ap.add_argument("--only", default="", help="comma-separated subset of: append, attention, rerotate, sink, "
-                    "qkv, unfused, motion, noise (default: all)")
+                    "qkv, cublas, unfused, motion, noise (default: all)")
     args = ap.parse_args()
     only = {x.strip() for x in args.only.split(",") if x.strip()}
 
@@ -142,6 +142,12 @@ def main():
                flops_per_call=gemm_flops, ms=_time(fused, 60, stream),
                extra={"bytes_min": int((w.nq * C + 3 * C * C) * 2 + w.nq * 3 * C * 2)})
     ybuf = torch.empty((1, w.nq, 3 * C), dtype=torch.bfloat16, device=dev)
+
+    def gemm_only(i):
+        torch.matmul(xs[i % nl][0], Wq.t(), out=ybuf[0])
+    if want("cublas"):
+        report("projection GEMM alone: torch.matmul (cuBLAS), bf16 out, no bias or RoPE", w.name,
+               flops_per_call=gemm_flops, ms=_time(gemm_only, 60, stream))
 
     def unfused(i):
         l = i % nl
