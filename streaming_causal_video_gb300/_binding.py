@@ -138,6 +138,25 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _dev(t, name, nbytes):
+    """Device pointer of a CUDA tensor, checked to reach at least `nbytes` bytes from its first
+    element within its storage (views such as packed q/k/v slices pass).  Raw integer pointers
+    and None pass through unchecked: the C ABI cannot see buffer sizes."""
+    if t is None or isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    avail = t.untyped_storage().nbytes() - t.storage_offset() * t.element_size()
+    if avail < nbytes:
+        raise ValueError("%s: %d bytes from its first element, the call touches %d" % (name, avail, nbytes))
+    return t.data_ptr()
+
+
+def _row_span(rows, stride, width, elem):
+    """Bytes from the first element of `rows` rows `stride` elements apart, `width` used each."""
+    return 0 if rows <= 0 else ((rows - 1) * stride + width) * elem
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -171,71 +190,101 @@ def visible_tokens(cfg: StreamConfig, chunk_index: int) -> int:
 
 
 def workspace_init(cfg, ws, stream=None):
-    _check(lib().sdv2_workspace_init(ctypes.byref(cfg), _ptr(ws), _stream(stream)), "sdv2_workspace_init")
+    _check(lib().sdv2_workspace_init(ctypes.byref(cfg), _dev(ws, "ws", workspace_bytes(cfg)), _stream(stream)),
+           "sdv2_workspace_init")
 
 
 def cache_reset(cfg, k_cache, v_cache, meta, stream=None):
-    _check(lib().sdv2_cache_reset(ctypes.byref(cfg), _ptr(k_cache), _ptr(v_cache), _ptr(meta), _stream(stream)),
-           "sdv2_cache_reset")
+    _, cb, mb, _, _ = _sizes(cfg)
+    _check(lib().sdv2_cache_reset(ctypes.byref(cfg), _dev(k_cache, "k_cache", cb), _dev(v_cache, "v_cache", cb),
+                                  _dev(meta, "meta", mb), _stream(stream)), "sdv2_cache_reset")
+
+
+def _sizes(cfg):
+    """Bytes each per-layer buffer spans: q_rot/out, caches, metadata, workspace, lse."""
+    qo = max(cfg.batch, 0) * max(cfg.heads, 0) * cfg.nq * 128 * 2
+    return qo, cache_bytes(cfg), meta_bytes(cfg), workspace_bytes(cfg), qo * 2
 
 
 def rope_append_kv(cfg, start_frame, chunk_index, q, k, v, q_rot, k_cache, v_cache, meta, ws, stream=None):
     B = cfg.batch
+    qo, cb, mb, wb, _ = _sizes(cfg)
+    C = max(cfg.heads, 0) * 128
+    span = _row_span(max(B, 0) * cfg.nq, cfg.qkv_token_stride or C, C, 2)
     _check(lib().sdv2_rope_append_kv(ctypes.byref(cfg), _i64_array(start_frame, B), _i64_array(chunk_index, B),
-                                     _ptr(q), _ptr(k), _ptr(v), _ptr(q_rot), _ptr(k_cache), _ptr(v_cache),
-                                     _ptr(meta), _ptr(ws), _stream(stream)), "sdv2_rope_append_kv")
+                                     _dev(q, "q", span), _dev(k, "k", span), _dev(v, "v", span),
+                                     _dev(q_rot, "q_rot", qo), _dev(k_cache, "k_cache", cb),
+                                     _dev(v_cache, "v_cache", cb), _dev(meta, "meta", mb), _dev(ws, "ws", wb),
+                                     _stream(stream)), "sdv2_rope_append_kv")
 
 
 def qkv_rope_append(cfg, start_frame, chunk_index, x, w_qkv, q_rot, k_cache, v_cache, meta, ws, bias=None,
                     x_token_stride=0, stream=None):
     """x: [B][Nq][H*D] bf16; w_qkv: [3*H*D][H*D] bf16; bias: fp32 [3*H*D] or None."""
     B = cfg.batch
+    qo, cb, mb, wb, _ = _sizes(cfg)
+    C = max(cfg.heads, 0) * 128
+    span = _row_span(max(B, 0) * cfg.nq, int(x_token_stride) or C, C, 2)
     _check(lib().sdv2_qkv_rope_append(ctypes.byref(cfg), _i64_array(start_frame, B), _i64_array(chunk_index, B),
-                                      _ptr(x), int(x_token_stride), _ptr(w_qkv), _ptr(bias), _ptr(q_rot),
-                                      _ptr(k_cache), _ptr(v_cache), _ptr(meta), _ptr(ws), _stream(stream)),
+                                      _dev(x, "x", span), int(x_token_stride), _dev(w_qkv, "w_qkv", 3 * C * C * 2),
+                                      _dev(bias, "bias", 3 * C * 4), _dev(q_rot, "q_rot", qo),
+                                      _dev(k_cache, "k_cache", cb), _dev(v_cache, "v_cache", cb),
+                                      _dev(meta, "meta", mb), _dev(ws, "ws", wb), _stream(stream)),
            "sdv2_qkv_rope_append")
 
 
 def chunk_attention(cfg, chunk_index, q_rot, k_cache, v_cache, out, ws, lse=None, scale=0.0, stream=None):
-    _check(lib().sdv2_chunk_attention(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch), _ptr(q_rot),
-                                      _ptr(k_cache), _ptr(v_cache), float(scale), _ptr(out), _ptr(lse), _ptr(ws),
-                                      _stream(stream)), "sdv2_chunk_attention")
+    qo, cb, _, wb, lb = _sizes(cfg)
+    _check(lib().sdv2_chunk_attention(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch),
+                                      _dev(q_rot, "q_rot", qo), _dev(k_cache, "k_cache", cb),
+                                      _dev(v_cache, "v_cache", cb), float(scale), _dev(out, "out", qo),
+                                      _dev(lse, "lse", lb), _dev(ws, "ws", wb), _stream(stream)),
+           "sdv2_chunk_attention")
 
 
 def chunk_attention_noalloc(cfg, chunk_index, q_rot, k_cache, v_cache, out, lse=None, scale=0.0, stream=None):
     """sdv2_chunk_attention_noalloc: the same attention without a caller-owned workspace."""
-    _check(lib().sdv2_chunk_attention_noalloc(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch), _ptr(q_rot),
-                                              _ptr(k_cache), _ptr(v_cache), float(scale), _ptr(out), _ptr(lse),
-                                              _stream(stream)), "sdv2_chunk_attention_noalloc")
+    qo, cb, _, _, lb = _sizes(cfg)
+    _check(lib().sdv2_chunk_attention_noalloc(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch),
+                                              _dev(q_rot, "q_rot", qo), _dev(k_cache, "k_cache", cb),
+                                              _dev(v_cache, "v_cache", cb), float(scale), _dev(out, "out", qo),
+                                              _dev(lse, "lse", lb), _stream(stream)), "sdv2_chunk_attention_noalloc")
 
 
 def motion_l2(frames, ssd, m=None, stream=None):
     """frames: uint8 [B][T+1][Hp][Wp][C] on the device; ssd: uint64-sized [B][T]; m: fp32 [B][T]."""
     B, T1, Hp, Wp, C = frames.shape
-    _check(lib().sdv2_motion_l2(_ptr(frames), B, T1 - 1, Hp, Wp, C, _ptr(ssd), _ptr(m), _stream(stream)),
-           "sdv2_motion_l2")
+    if not frames.is_contiguous():
+        raise ValueError("frames must be contiguous")
+    n = B * max(T1 - 1, 0)
+    _check(lib().sdv2_motion_l2(_dev(frames, "frames", frames.numel()), B, T1 - 1, Hp, Wp, C, _dev(ssd, "ssd", n * 8),
+                                _dev(m, "m", n * 4), _stream(stream)), "sdv2_motion_l2")
 
 
 def rope_refresh_rerotate(cfg, chunk_index, k_cache, meta, stream=None):
-    _check(lib().sdv2_rope_refresh_rerotate(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch), _ptr(k_cache),
-                                            _ptr(meta), _stream(stream)), "sdv2_rope_refresh_rerotate")
+    _, cb, mb, _, _ = _sizes(cfg)
+    _check(lib().sdv2_rope_refresh_rerotate(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch),
+                                            _dev(k_cache, "k_cache", cb), _dev(meta, "meta", mb), _stream(stream)),
+           "sdv2_rope_refresh_rerotate")
 
 
 def sink_update(cfg, chunk_index, update, k_cache, v_cache, meta, stream=None):
     upd = (ctypes.c_int32 * cfg.batch)(*[int(u) for u in update])
-    _check(lib().sdv2_sink_update(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch), upd, _ptr(k_cache),
-                                  _ptr(v_cache), _ptr(meta), _stream(stream)), "sdv2_sink_update")
+    _, cb, mb, _, _ = _sizes(cfg)
+    _check(lib().sdv2_sink_update(ctypes.byref(cfg), _i64_array(chunk_index, cfg.batch), upd,
+                                  _dev(k_cache, "k_cache", cb), _dev(v_cache, "v_cache", cb), _dev(meta, "meta", mb),
+                                  _stream(stream)), "sdv2_sink_update")
 
 
 def noise_from_motion(ctl, m, rate, state=None, stream=None):
     """m, rate: device fp32 [B][T]; state: device fp32 [B] or None."""
     B, T = m.shape
-    _check(lib().sdv2_noise_from_motion(ctypes.byref(ctl), _ptr(m), B, T, _ptr(state), _ptr(rate), _stream(stream)),
-           "sdv2_noise_from_motion")
+    _check(lib().sdv2_noise_from_motion(ctypes.byref(ctl), _dev(m, "m", B * T * 4), B, T, _dev(state, "state", B * 4),
+                                        _dev(rate, "rate", B * T * 4), _stream(stream)), "sdv2_noise_from_motion")
 
 
 def check_device_error(ws, stream=None):
-    _check(lib().sdv2_check_device_error(_ptr(ws), _stream(stream)), "sdv2_check_device_error")
+    _check(lib().sdv2_check_device_error(_dev(ws, "ws", 16), _stream(stream)), "sdv2_check_device_error")
 
 
 def set_wait_timeout_ns(ns: int):

@@ -122,3 +122,22 @@ def test_status_strings():
     L = sd.lib()
     assert L.sdv2_status_string(0) == b"ok"
     assert L.sdv2_status_string(4) == b"device wait timed out"
+
+
+def test_binding_checks_tensor_device_and_extent_before_the_call():
+    """The binding turns a host tensor, or one whose storage ends before the bytes an entry point
+    touches, into ValueError on the host, before any C call (raw integer pointers are not
+    checked: the C ABI cannot see buffer sizes)."""
+    import torch
+    from streaming_causal_video_gb300 import _binding as b
+    assert b._row_span(0, 7, 5, 2) == 0
+    assert b._row_span(3, 10, 4, 2) == (2 * 10 + 4) * 2          # last row starts 20 elements in
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        b._dev(torch.zeros(4), "x", 16)
+    assert b._dev(FAKE, "x", 1 << 40) == FAKE and b._dev(None, "x", 1) is None
+    cfg = sd.StreamConfig.make(**stream_config_dict(WORKLOADS["tiny"]))
+    host = torch.zeros(16)
+    with pytest.raises(ValueError, match="q_rot must be a CUDA tensor"):
+        sd.chunk_attention(cfg, [0], host, FAKE, FAKE, FAKE, FAKE, stream=0)
+    with pytest.raises(ValueError, match="k_cache must be a CUDA tensor"):
+        sd.sink_update(cfg, [0], [1], host, FAKE, FAKE, stream=0)

@@ -163,3 +163,24 @@ def test_two_sessions_on_two_streams_equal_serial_runs():
     for c in range(chunks):
         np.testing.assert_array_equal(ca[c], sa_[c], err_msg="session a, chunk %d" % c)
         np.testing.assert_array_equal(cb[c], sb_[c], err_msg="session b, chunk %d" % c)
+
+
+def test_undersized_or_offset_buffers_are_refused_on_the_host():
+    """A buffer whose storage ends before the bytes a call touches raises ValueError in the
+    binding; nothing is launched (the error word stays clear and a correct call follows)."""
+    cfg = config(W)
+    sess = sd.StreamSession(cfg, 1, list(W.start_frames), "cuda")
+    L = sess.layers[0]
+    q, k, v = (torch.randn((W.batch, W.nq, W.heads, 128), device="cuda").to(torch.bfloat16) for _ in range(3))
+    short = torch.empty(sess.q_rot.numel() - 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError, match="q_rot"):
+        sd.rope_append_kv(cfg, W.start_frames, [0] * W.batch, q, k, v, short, L.k, L.v, L.meta, sess.ws)
+    with pytest.raises(ValueError, match="k_cache"):
+        sd.chunk_attention(cfg, [0] * W.batch, sess.q_rot, L.k.view(-1)[64:], L.v, sess.out, sess.ws)
+    with pytest.raises(ValueError, match="q"):
+        sd.rope_append_kv(cfg, W.start_frames, [0] * W.batch, q[:, 1:], k, v, sess.q_rot, L.k, L.v, L.meta, sess.ws)
+    sd.rope_append_kv(cfg, W.start_frames, [0] * W.batch, q, k, v, sess.q_rot, L.k, L.v, L.meta, sess.ws)
+    sd.chunk_attention(cfg, [0] * W.batch, sess.q_rot, L.k, L.v, sess.out, sess.ws)
+    torch.cuda.synchronize()
+    sd.check_device_error(sess.ws)
+    assert torch.isfinite(sess.out.float()).all()
