@@ -202,8 +202,8 @@ def cache_reset(cfg, k_cache, v_cache, meta, stream=None):
 
 def _sizes(cfg):
     """Bytes each per-layer buffer spans: q_rot/out, caches, metadata, workspace, lse."""
-    qo = max(cfg.batch, 0) * max(cfg.heads, 0) * cfg.nq * 128 * 2
-    return qo, cache_bytes(cfg), meta_bytes(cfg), workspace_bytes(cfg), qo * 2
+    rows = max(cfg.batch, 0) * max(cfg.heads, 0) * cfg.nq          # (stream, head, query) rows
+    return rows * 128 * 2, cache_bytes(cfg), meta_bytes(cfg), workspace_bytes(cfg), rows * 4
 
 
 def rope_append_kv(cfg, start_frame, chunk_index, q, k, v, q_rot, k_cache, v_cache, meta, ws, stream=None):

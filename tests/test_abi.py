@@ -141,3 +141,15 @@ def test_binding_checks_tensor_device_and_extent_before_the_call():
         sd.chunk_attention(cfg, [0], host, FAKE, FAKE, FAKE, FAKE, stream=0)
     with pytest.raises(ValueError, match="k_cache must be a CUDA tensor"):
         sd.sink_update(cfg, [0], [1], host, FAKE, FAKE, stream=0)
+
+
+def test_binding_buffer_sizes_match_the_header():
+    """Bytes the binding requires of each buffer, against the layouts include/sdv2.h states:
+    q_rot/out [B][H][Nq][128] bf16, lse [B][H][Nq] fp32, caches and metadata per the size queries."""
+    from streaming_causal_video_gb300 import _binding as b
+    w = WORKLOADS["wan13b_480p"]
+    cfg = sd.StreamConfig.make(**stream_config_dict(w))
+    qo, cb, mb, wb, lb = b._sizes(cfg)
+    assert qo == w.batch * w.heads * w.nq * 128 * 2
+    assert lb == w.batch * w.heads * w.nq * 4
+    assert cb == sd.cache_bytes(cfg) and mb == sd.meta_bytes(cfg) and wb == sd.workspace_bytes(cfg)
