@@ -443,6 +443,8 @@ sdv2_status sdv2_rope_refresh_rerotate(const sdv2_stream_cfg* c, const int64_t* 
         return fail(SDV2_ERR_INVALID_ARG, "k_cache and meta must be non-null and 16-byte aligned");
     if (c->batch > sdv2::kMaxCacheStreams) return fail(SDV2_ERR_UNSUPPORTED, "more than 64 streams");
     if (c->rope_t / 2 > sdv2::kMaxTimePairsPerAxis) return fail(SDV2_ERR_UNSUPPORTED, "rope_t > 128");
+    for (int b = 0; b < c->batch; ++b)
+        if (chunk_index[b] < 0) return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be >= 0", b);
     if ((s = check_device()) != SDV2_OK) return s;
     sdv2::RerotateParams p{};
     p.k_cache = static_cast<uint16_t*>(k_cache);
@@ -459,7 +461,6 @@ sdv2_status sdv2_rope_refresh_rerotate(const sdv2_stream_cfg* c, const int64_t* 
     p.shift = static_cast<int64_t>(c->chunk_frames) * R;
     bool any = false;
     for (int b = 0; b < c->batch; ++b) {
-        if (chunk_index[b] < 0) return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be >= 0", b);
         p.active[b] = (R > 0 && chunk_index[b] > 0 && chunk_index[b] % R == 0) ? 1 : 0;
         p.limit[b] = chunk_index[b] * c->chunk_frames;
         any = any || p.active[b];

@@ -153,3 +153,47 @@ def test_binding_buffer_sizes_match_the_header():
     assert qo == w.batch * w.heads * w.nq * 128 * 2
     assert lb == w.batch * w.heads * w.nq * 4
     assert cb == sd.cache_bytes(cfg) and mb == sd.meta_bytes(cfg) and wb == sd.workspace_bytes(cfg)
+
+
+def test_next_row_entry_points_validate_on_the_host():
+    """The fused projection, the re-rotation, the sink update and the noise controller reject
+    bad arguments with a status and a message before touching the device."""
+    c = _cfg()
+    C = c.heads * 128
+    args = lambda **o: dict(dict(x=FAKE, stride=0, w=FAKE, bias=None, start=[0], chunk=[0]), **o)
+
+    def qkv(a):
+        return _status(sd.qkv_rope_append, c, a["start"], a["chunk"], a["x"], a["w"], FAKE, FAKE, FAKE, FAKE, FAKE,
+                       a["bias"], a["stride"], 0)
+    assert qkv(args(x=FAKE + 8)) == 1                       # misaligned x
+    assert qkv(args(w=None)) == 1
+    assert qkv(args(stride=C - 8)) == 1                     # token stride below H*D
+    assert qkv(args(stride=C + 4)) == 1                     # not a multiple of 8
+    assert b"x_token_stride" in sd.lib().sdv2_last_error()
+    assert qkv(args(bias=FAKE + 4)) == 1                    # bias not 16-byte aligned
+    assert qkv(args(chunk=[-1])) == 1 and qkv(args(start=[-5])) == 1
+    rr = _cfg(refresh_chunks=3)
+    assert _status(sd.rope_refresh_rerotate, rr, [3], None, FAKE, 0) == 1
+    assert _status(sd.rope_refresh_rerotate, rr, [3], FAKE, FAKE + 8, 0) == 1
+    assert _status(sd.rope_refresh_rerotate, rr, [-1], FAKE, FAKE, 0) == 1
+    assert b"chunk_index" in sd.lib().sdv2_last_error()
+    assert _status(sd.rope_refresh_rerotate, _cfg(batch=65), [3] * 65, FAKE, FAKE, 0) == 2
+    s = _cfg(sink_frames=3, window_frames=4, chunk_frames=3)
+    assert _status(sd.sink_update, s, [0], [1], FAKE, FAKE, FAKE, 0) == 1      # 3 frames < 2 * sink
+    assert b"2*sink_frames" in sd.lib().sdv2_last_error()
+    assert _status(sd.sink_update, s, [-1], [1], FAKE, FAKE, FAKE, 0) == 1
+    assert _status(sd.sink_update, s, [5], [1], None, FAKE, FAKE, 0) == 1
+    sd.sink_update(s, [5], [0], FAKE, FAKE, FAKE, 0)                             # nothing to do: ok
+    sd.sink_update(_cfg(sink_frames=0), [5], [1], FAKE, FAKE, FAKE, 0)          # no sink: ok
+    L = sd.lib()
+
+    def noise(ctl, B=2, T=5, m=FAKE, rate=FAKE):
+        return L.sdv2_noise_from_motion(ctypes.byref(ctl), m, B, T, None, rate, None)
+    good = dict(motion_lo=2.0, motion_hi=12.0, rate_lo=0.1, rate_hi=0.9, ema=0.5, more_noise_when_fast=1)
+    mk = lambda **o: sd.NoiseCtl(**dict(good, **o))
+    assert noise(mk(), B=0) == 1 and noise(mk(), T=0) == 1
+    assert noise(mk(motion_hi=2.0)) == 1 and noise(mk(motion_lo=float("nan"))) == 1
+    assert noise(mk(rate_lo=-0.1)) == 1 and noise(mk(rate_hi=float("inf"))) == 1
+    assert noise(mk(ema=1.0)) == 1 and noise(mk(ema=-0.1)) == 1
+    assert noise(mk(), m=FAKE + 2) == 1 and noise(mk(), rate=None) == 1
+    assert noise(mk()) not in (0, 1)          # valid arguments reach the device check (no GPU here)
