@@ -20,7 +20,9 @@
  *    launches nothing and returns SDV2_ERR_INVALID_ARG or SDV2_ERR_UNSUPPORTED.  A failed
  *    launch returns SDV2_ERR_CUDA.  sdv2_last_error() gives a one-line reason (per thread).
  *  - Device pointers must be 16-byte aligned.
- *  - bf16 means IEEE binary32 truncated to its upper 16 bits (bfloat16), stored as uint16.
+ *  - bf16 means bfloat16: the upper 16 bits of the IEEE binary32 layout (sign, 8 exponent
+ *    bits, 7 mantissa bits), stored as uint16.  Every bf16 the library writes is rounded to
+ *    nearest, ties to even.
  *
  * Notation (stream configuration): B streams, H heads, D = head_dim = 128, HW = grid_h*grid_w
  * tokens per latent frame, F frames per chunk, Nq = F*HW queries per chunk, F_s sink frames,
@@ -262,7 +264,8 @@ sdv2_status sdv2_rope_refresh_rerotate(const sdv2_stream_cfg* cfg, const int64_t
                                        void* k_cache, void* meta, void* stream);
 
 /*
- * Sink update ("StreamDiffusionV2" gist summary 2.A.2: sink tokens follow recent visual
+ * Sink update ("StreamDiffusionV2: A Streaming System for Dynamic and Interactive Video
+ * Generation", technical summary section 2, part A item 2: sink tokens follow recent visual
  * context).  Read here as: the sink is replaced by copies of the F_s most recently appended
  * frames.  For every stream b with update[b] != 0 (host int32 [B]), after chunk chunk_index[b]
  * has been appended (n = (c+1)*F frames), sink slot s (0 <= s < F_s) receives the k and v rows
@@ -274,7 +277,8 @@ sdv2_status sdv2_sink_update(const sdv2_stream_cfg* cfg, const int64_t* chunk_in
                              void* stream);
 
 /* Motion-aware noise controller: a declared monotone map (the pages give no formula and
- * disagree on its direction: gist summary 2.A.3 vs review page section 三). */
+ * disagree on its direction: the StreamDiffusionV2 technical summary, section 2 part A item 3,
+ * vs the review page, section 三). */
 typedef struct {
     float motion_lo, motion_hi;  /* RMS motion (0..255 scale) mapped to the low / high end     */
     float rate_lo, rate_hi;      /* noise rates at the two ends (>= 0)                          */

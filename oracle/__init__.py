@@ -9,7 +9,7 @@ What each function follows (pages are cited by title and section):
   Positional Encoding Using a Global Time Index", technical summary 2(나): each generated block
   computes its tokens' time index locally from the block's start frame (the global time
   index), so no gather of the whole sequence is needed.  The periodic offset reset of
-  "StreamDiffusionV2" (review page, section 三, "RoPE 刷新"; gist summary 2.A.2) is read as: the
+  "StreamDiffusionV2" (review page, section 三, "RoPE 刷新"; technical summary section 2 part A item 2) is read as: the
   chunk offset inside the time index restarts every R chunks, t = S + F*(c mod R) + i.
 * FrameListCache -- the same review page, section 三 ("Sink Token 引导的滚动 KV 缓存"): the KV of
   the first frames is kept as a sink, and a fixed-size window of the most recent frames rolls.
@@ -29,7 +29,7 @@ What each function follows (pages are cited by title and section):
   primitive), for the fused projection + Causal-RoPE path of the Causal-RoPE page, technical
   summary 2(다); its output is rotated with rope_ideal.
 * noise -- the motion-to-noise-rate map.  PARITY UNPINNED with respect to the pages: they give
-  no formula and disagree on its direction (gist summary 2.A.3 vs review page section 三); the
+  no formula and disagree on its direction (technical summary section 2 part A item 3 vs review page section 三); the
   map is a declared reading, pinned only to its own stated properties (monotone, end points,
   direction flag, smoothing closed form).
 """

@@ -5,9 +5,9 @@
 //   offset"): when the time offset resets by F*R, the keys already in the rolling window are
 //   turned back by the same F*R on the time axis, so that distances between the new chunk and
 //   the window stay what they were (positions stay continuous across the reset).
-// * Sink update ("StreamDiffusionV2" gist summary 2.A.2: sink tokens are updated from recent
-//   visual context): the sink slots receive copies of the most recently appended frames.
-// * Noise controller (review page section 三 / gist summary 2.A.3): a monotone map from the
+// * Sink update ("StreamDiffusionV2" technical summary, section 2 part A item 2: sink tokens are
+//   updated from recent visual context): the sink slots receive copies of the most recently appended frames.
+// * Noise controller (review page section 三 / technical summary section 2 part A item 3): a monotone map from the
 //   per-frame motion magnitude to a noise rate, with optional exponential smoothing.
 //
 // All three are HBM- or latency-bound and tiny next to attention; they use 16-byte vectors

@@ -2,7 +2,7 @@
 //
 // "StreamDiffusionV2" review page, section 二 (table of innovations: L2 motion estimate ->
 // adaptive noise rate) and section 三 (motion-aware noise controller: compute the motion
-// magnitude of adjacent frames).  The gist summary (2.A.3) mentions optical flow as one way of
+// magnitude of adjacent frames).  The technical summary (section 2 part A item 3) mentions optical flow as one way of
 // estimating the motion strength; the raw pixel L2 distance is the plain reading of "L2".
 //
 // Work split: each block owns a slab of 16-byte vectors of the frame and a run of consecutive
