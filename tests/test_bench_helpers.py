@@ -78,3 +78,42 @@ def test_clock_samples_give_median_max_and_active_reasons():
     r = _summary(["1500, 2070, 900, 0x8, Active, Not Active, Active, Not Active"])
     assert r["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
     assert bench.ClockSampler(0).stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+# The text of get_encode_tiled in the build the ncu traffic record was captured on.
+_CAPTURED_GET_ENCODE_TILED = '''EncodeTiledFn get_encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}'''
+
+
+def test_traffic_record_differs_from_its_capture_only_in_the_encoder_lookup():
+    """The record's changes_since_capture claim, checked: with the captured text of
+    get_encode_tiled put back, the current sources hash to the captured hash."""
+    path = os.path.join(bench.ROOT, "profiles", "chunk_attention_wan13b_480p.json")
+    with open(path) as fh:
+        rec = json.load(fh)
+    if "captured_source_hash" not in rec:
+        return
+    start_tag = "EncodeTiledFn get_encode_tiled()"
+
+    def captured(f):
+        text = _read(f)
+        if f != "attention.cu":
+            return text
+        a = text.index(start_tag)
+        b = text.index("    return fn;\n}", a) + len("    return fn;\n}")
+        return text[:a] + _CAPTURED_GET_ENCODE_TILED + text[b:]
+    assert bench.attention_source_hash(captured) == rec["captured_source_hash"]
+    assert bench.attention_source_hash() == rec["source_hash"]
