@@ -151,15 +151,19 @@ sdv2_status check_device()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return fail(SDV2_ERR_CUDA, "cudaGetDevice failed");
-    static int8_t known[64] = {};
+    // 0 = not looked up yet, 1 = sm_103, -1 = another device; threads racing on the first
+    // lookup store the same value
+    static std::atomic<int8_t> known[64];
     if (dev < 0 || dev >= 64) return fail(SDV2_ERR_UNSUPPORTED, "device index %d out of range", dev);
-    if (known[dev] == 0) {
+    int8_t k = known[dev].load(std::memory_order_relaxed);
+    if (k == 0) {
         int major = 0, minor = 0;
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-        known[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        k = (major == 10 && minor == 3) ? 1 : -1;
+        known[dev].store(k, std::memory_order_relaxed);
     }
-    if (known[dev] < 0) return fail(SDV2_ERR_UNSUPPORTED, "the library is built for sm_103a (GB300) only");
+    if (k < 0) return fail(SDV2_ERR_UNSUPPORTED, "the library is built for sm_103a (GB300) only");
     return SDV2_OK;
 }
 
