@@ -14,8 +14,12 @@ roofline: the attention kernel, its flops per launch over its mean launch time (
 cpu_baseline / --impl reference: the CPU oracle on the same workload, on a bounded sample of
           query rows (its cost per row is fixed at a given key count).
 
+roofline_rope_append: the same for sdv2_rope_append_kv against the measured HBM copy bandwidth.
+workloads: steady-state lines of the 1.3B-720p, 14B-480p and stream-batch shapes (same step and
+          timing code, a few steps each), each with the oracle's attention on sampled rows.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+       [--workload NAME] [--no-e2e] [--no-cpu-baseline] [--no-workloads] [--workload-steps K]
 """
 import argparse
 import hashlib
@@ -174,8 +178,13 @@ def code_only(text):
     return " ".join(text.split())
 
 
+ATTN_SECTION = ("// ---- chunk attention", "// ---- motion")
+
+
 def attention_source_hash(read=None):
-    """Hash of the code (not the comments) the attention kernel is built from."""
+    """Hash of the code (not the comments) the attention kernel is built from: attention.cu,
+    ptx.cuh, tmem_io.cuh and the chunk-attention section of internal.h (the other sections of
+    that header describe other kernels)."""
     h = hashlib.sha256()
     for f in ("attention.cu", "ptx.cuh", "tmem_io.cuh", "internal.h"):
         if read is None:
@@ -183,6 +192,9 @@ def attention_source_hash(read=None):
                 text = fh.read()
         else:
             text = read(f)
+        if f == "internal.h":
+            a = text.index(ATTN_SECTION[0])
+            text = text[a:text.index(ATTN_SECTION[1], a)]
         h.update(code_only(text).encode())
     return h.hexdigest()[:16]
 
@@ -230,96 +242,194 @@ def oracle_sample(w, seconds_target, seed=0, max_rows=4096):
     return flops, t_total, rows_done, oracle.num_threads()
 
 
+def oracle_rope_append_sample(w, seconds_target):
+    """Time the oracle's Causal-RoPE + cache append of whole chunks of workload w: rope_spec of
+    the chunk's q and k (every head) and FrameListCache.append of its frames.  Returns
+    (chunks, seconds, bytes per chunk)."""
+    import oracle
+    from synth_inputs import qkv_chunk_bits
+    q, k, v = qkv_chunk_bits(w, 1, 0)
+    so = oracle.StreamOracle(w, w.start_frames[0])
+    done, t_total, c = 0, 0.0, 0
+    while t_total < seconds_target or done == 0:
+        t0 = time.perf_counter()
+        so.append_chunk(c, q[0], k[0], v[0])
+        t_total += time.perf_counter() - t0
+        done += 1
+        c += 1
+    return done, t_total, 1536.0 * w.nq * w.heads
+
+
+def oracle_motion_sample(frames_np, seconds_target):
+    """Time the oracle's exact SSD over the given frames [B][T+1][...] repeatedly.  Returns
+    (passes, seconds, bytes per pass)."""
+    import oracle
+    done, t_total = 0, 0.0
+    while t_total < seconds_target or done == 0:
+        t0 = time.perf_counter()
+        oracle.motion_ssd(frames_np)
+        t_total += time.perf_counter() - t0
+        done += 1
+    return done, t_total, float(frames_np.size)
+
+
 # ------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------
 
+class SteadyStream:
+    """Device state of one workload at steady state (full sink + window in every layer's cache),
+    and one bench step: motion over the chunk's video frames, then for each denoise step and
+    layer, sdv2_rope_append_kv followed by sdv2_chunk_attention."""
+
+    def __init__(self, w, dev, stream):
+        import torch
+        import streaming_causal_video_gb300 as sd
+        from synth_inputs import motion_frames_host
+        self.sd = sd
+        self.w = w
+        self.stream = stream
+        self.cfg = sd.StreamConfig.make(**stream_config_dict(w))
+        B, H, D, nq = w.batch, w.heads, w.head_dim, w.nq
+        self.sess = sd.StreamSession(self.cfg, w.layers, w.start_frames, dev, stream)
+        g = torch.Generator(device=dev).manual_seed(w.seed)
+        self.qkv = [tuple(torch.randn((B, nq, H, D), generator=g, device=dev, dtype=torch.float32)
+                          .to(torch.bfloat16) for _ in range(3)) for _ in range(w.layers)]
+        self.outs = [torch.empty((B, nq, H, D), dtype=torch.bfloat16, device=dev) for _ in range(w.layers)]
+        self.vf = VIDEO_FRAMES_PER_LATENT * w.chunk_frames
+        Hp, Wp, Cc = VIDEO_SHAPE
+        self.frames = motion_frames_host(B, self.vf + 1, Hp, Wp, Cc, seed=w.seed, device=dev)
+        self.ssd = torch.empty((B, self.vf), dtype=torch.int64, device=dev)
+        self.mrms = torch.empty((B, self.vf), dtype=torch.float32, device=dev)
+        steady = 0
+        while sd.visible_tokens(self.cfg, steady) < w.slots * w.hw:
+            steady += 1
+        for c in range(steady):
+            for l in range(w.layers):
+                q, k, v = self.qkv[l]
+                self.sess.layer_step(l, [c] * B, q, k, v, out=self.outs[l], stream=stream)
+        stream.synchronize()
+        sd.check_device_error(self.sess.ws, stream)
+        self.chunk = steady
+        self.attn_flops = 4.0 * H * D * nq * sd.visible_tokens(self.cfg, steady) * B
+        self.rope_bytes = 1536.0 * B * nq * H          # read q, k, v; write q_rot, k, v rows
+        self.launches_per_step = 3 + 2 * w.denoise_steps * w.layers
+
+    def step(self, attn_ev=None, rope_ev=None):
+        """One chunk; returns its attention flops.  attn_ev / rope_ev, if lists, receive a pair
+        of CUDA events around every attention / rope_append call (recorded on the launch
+        stream)."""
+        import torch
+        sd, w, st, S = self.sd, self.w, self.stream, self.sess
+        c = self.chunk
+        B = w.batch
+
+        def ev():
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(st)
+            return e
+        sd.motion_l2(self.frames, self.ssd, self.mrms, stream=st)
+        for _s in range(w.denoise_steps):
+            for l in range(w.layers):
+                q, k, v = self.qkv[l]
+                L = S.layers[l]
+                r0 = ev() if rope_ev is not None else None
+                sd.rope_append_kv(self.cfg, w.start_frames, [c] * B, q, k, v, S.q_rot, L.k, L.v, L.meta, S.ws, st)
+                a0 = ev() if (rope_ev is not None or attn_ev is not None) else None
+                sd.chunk_attention(self.cfg, [c] * B, S.q_rot, L.k, L.v, self.outs[l], S.ws, stream=st)
+                if rope_ev is not None:
+                    rope_ev.append((r0, a0))
+                if attn_ev is not None:
+                    attn_ev.append((a0, ev()))
+        self.chunk += 1
+        return w.denoise_steps * w.layers * self.attn_flops
+
+    def close(self):
+        import torch
+        self.sd.check_device_error(self.sess.ws, self.stream)
+        del self.sess, self.qkv, self.outs, self.frames
+        torch.cuda.empty_cache()
+
+
+def timed_steps(state, steps, dist, dev, clock_gpu, attn_ev=None, rope_ev=None):
+    """Barrier + synchronize, time `steps` steps with CUDA events on the launch stream, barrier +
+    synchronize; clocks sampled during the region.  Returns (flops, ms max over ranks, clocks)."""
+    import torch
+    clocks = ClockSampler(clock_gpu)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(state.stream)
+    flops = 0.0
+    for _ in range(steps):
+        flops += state.step(attn_ev, rope_ev)
+    t1.record(state.stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clk = clocks.stop()
+    return flops, dist.max(t0.elapsed_time(t1)), clk
+
+
+def measure_other_workload(name, steps, warmup, dist, dev, stream, oracle_seconds):
+    """Steady-state attention TFLOP/s and latent frames/s of another workload (same step and
+    timing code as the headline), with the oracle's attention on sampled rows beside it."""
+    w = WORKLOADS[name]
+    state = SteadyStream(w, dev, stream)
+    for _ in range(warmup):
+        state.step()
+    stream.synchronize()
+    attn_ev = []
+    flops, ms, clk = timed_steps(state, steps, dist, dev, dist.local, attn_ev=attn_ev)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
+    splits = state.sd.last_kv_splits()
+    state.close()
+    res = {"workload": describe(w), "steps": steps, "ms_per_step": round(ms / steps, 3),
+           "attention_tflops": round(flops * dist.world / (ms * 1e-3) / 1e12, 3),
+           "latent_frames_per_s": round(steps * w.chunk_frames * w.batch * dist.world / (ms * 1e-3), 3),
+           "attention_ms_per_call": round(attn_ms, 4),
+           "attention_call_tflops": round(state.attn_flops / (attn_ms * 1e-3) / 1e12, 2),
+           "kv_splits": splits, "clocks": clk}
+    if dist.world == 1 and oracle_seconds > 0:
+        f, secs, rows, threads = oracle_sample(w, oracle_seconds, seed=7)
+        res["cpu_baseline"] = {"value": round(f / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+                               "kind": "oracle",
+                               "sample": "fp64 oracle attention of %d query rows against the steady-state %d keys "
+                                         "(%.1f s)" % (rows, w.slots * w.hw, secs)}
+    return res
+
+
 def run_ours(args, dist):
     import torch
     import streaming_causal_video_gb300 as sd
-    from synth_inputs import motion_frames_host
 
     torch.cuda.set_device(dist.local)
     dev = torch.device("cuda", dist.local)
     w = WORKLOADS[args.workload]
-    cfg = sd.StreamConfig.make(**stream_config_dict(w))
     B, H, D, nq = w.batch, w.heads, w.head_dim, w.nq
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
 
-    sess = sd.StreamSession(cfg, w.layers, w.start_frames, dev, stream)
-    g = torch.Generator(device=dev).manual_seed(w.seed)
-    qkv = [tuple(torch.randn((B, nq, H, D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
-                 for _ in range(3)) for _ in range(w.layers)]
-    outs = [torch.empty((B, nq, H, D), dtype=torch.bfloat16, device=dev) for _ in range(w.layers)]
-    vf = VIDEO_FRAMES_PER_LATENT * w.chunk_frames
-    Hp, Wp, Cc = VIDEO_SHAPE
-    frames = motion_frames_host(B, vf + 1, Hp, Wp, Cc, seed=w.seed, device=dev)
-    ssd = torch.empty((B, vf), dtype=torch.int64, device=dev)
-    mrms = torch.empty((B, vf), dtype=torch.float32, device=dev)
-
-    steady = 0
-    while sd.visible_tokens(cfg, steady) < w.slots * w.hw:
-        steady += 1
-    # bring every layer's cache to the steady state (full sink + window)
-    for c in range(steady):
-        for l in range(w.layers):
-            q, k, v = qkv[l]
-            sess.layer_step(l, [c] * B, q, k, v, out=outs[l], stream=stream)
-    stream.synchronize()
-    sd.check_device_error(sess.ws, stream)
-
-    flops_per_call = [4.0 * H * D * nq * sd.visible_tokens(cfg, c) * B for c in range(steady + 1)]
-    chunk = [steady]
-
-    def step(ev_pairs=None):
-        c = chunk[0]
-        sd.motion_l2(frames, ssd, mrms, stream=stream)
-        for _s in range(w.denoise_steps):
-            for l in range(w.layers):
-                q, k, v = qkv[l]
-                sd.rope_append_kv(cfg, w.start_frames, [c] * B, q, k, v, sess.q_rot, sess.layers[l].k,
-                                  sess.layers[l].v, sess.layers[l].meta, sess.ws, stream)
-                if ev_pairs is not None:
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                sd.chunk_attention(cfg, [c] * B, sess.q_rot, sess.layers[l].k, sess.layers[l].v, outs[l],
-                                   sess.ws, stream=stream)
-                if ev_pairs is not None:
-                    e1.record(stream)
-                    ev_pairs.append((e0, e1))
-        chunk[0] += 1
-        return w.denoise_steps * w.layers * flops_per_call[-1]
-
-    launches_per_step = 3 + 2 * w.denoise_steps * w.layers
+    state = SteadyStream(w, dev, stream)
+    cfg, sess, qkv, outs = state.cfg, state.sess, state.qkv, state.outs
+    frames, ssd, mrms, vf = state.frames, state.ssd, state.mrms, state.vf
+    flops_per_call = state.attn_flops
+    launches_per_step = state.launches_per_step
     warmup = max(3, args.warmup)
     for _ in range(warmup):
-        step()
+        state.step()
     stream.synchronize()
     sd.check_device_error(sess.ws, stream)
 
-    # ---- device-resident timed region
-    clocks = ClockSampler(dist.local)
-    clocks.start()
-    ev_pairs = []
-    dist.barrier()
-    torch.cuda.synchronize(dev)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    flops = 0.0
-    for _ in range(args.steps):
-        flops += step(ev_pairs)
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    dist.barrier()
-    clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
+    # ---- device-resident timed region (events around every attention and rope_append call)
+    attn_ev, rope_ev = [], []
+    flops, ms_max, clk = timed_steps(state, args.steps, dist, dev, dist.local, attn_ev=attn_ev, rope_ev=rope_ev)
     sd.check_device_error(sess.ws, stream)
-    ms_max = dist.max(ms)
-    attn_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    rope_ms = [a.elapsed_time(b) for a, b in rope_ev]
     attn_mean_ms = statistics.mean(attn_ms)
+    rope_mean_ms = statistics.mean(rope_ms)
     total_flops = flops * dist.world
     value = total_flops / (ms_max * 1e-3) / 1e12
     latent_fps = args.steps * w.chunk_frames * B * dist.world / (ms_max * 1e-3)
@@ -353,7 +463,7 @@ def run_ours(args, dist):
         counter = [0]
 
         def e2e_step():
-            c = chunk[0]
+            c = state.chunk
             with torch.cuda.stream(h2d_stream):
                 frames.copy_(h_frames, non_blocking=True)
                 fr_ready = torch.cuda.Event()
@@ -391,8 +501,8 @@ def run_ours(args, dist):
                         d2h_stream.wait_event(out_ready[l])
                         h_out[l].copy_(outs[l], non_blocking=True)
                         out_free[l].record(d2h_stream)
-            chunk[0] += 1
-            return w.denoise_steps * w.layers * flops_per_call[-1]
+            state.chunk += 1
+            return w.denoise_steps * w.layers * flops_per_call
 
         for _ in range(warmup):
             e2e_step()
@@ -421,17 +531,27 @@ def run_ours(args, dist):
                "ms_per_step": round(ms2 / args.steps, 3),
                "latent_frames_per_s": round(args.steps * w.chunk_frames * B * dist.world / (ms2 * 1e-3), 3),
                "copies": "pinned host buffers; H2D and D2H on two copy streams overlapped with compute"}
+        del h_qkv, h_out, d_in
 
     peaks, peak_src = load_peaks()
     peak = peak_value(peaks, "bf16_tflops_sustained") or PEAK_FALLBACK["bf16_tflops_sustained"]
-    attn_flops = flops_per_call[-1]
-    achieved = attn_flops / (attn_mean_ms * 1e-3) / 1e12
+    hbm = peak_value(peaks, "hbm_gbs") or PEAK_FALLBACK["hbm_gbs"]
+    achieved = flops_per_call / (attn_mean_ms * 1e-3) / 1e12
     traffic = profiled_traffic(args.workload)
     roofline = {"bound": "tensor", "kernel": "chunk_attention_kernel", "achieved": round(achieved, 2),
                 "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % peak_src,
-                "flops_per_launch": attn_flops, "mean_launch_ms": round(attn_mean_ms, 4),
+                "flops_per_launch": flops_per_call, "mean_launch_ms": round(attn_mean_ms, 4),
                 "launches_timed": len(attn_ms)}
+    rope_gbs = state.rope_bytes / (rope_mean_ms * 1e-3) / 1e9
+    roofline_rope = {"bound": "hbm", "kernel": "rope_append_kernel", "achieved": round(rope_gbs, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(rope_gbs / hbm, 4), "traffic": None,
+                     "peak_source": "%s hbm_gbs" % peak_src,
+                     "bytes_per_launch": state.rope_bytes, "mean_launch_ms": round(rope_mean_ms, 5),
+                     "launches_timed": len(rope_ms), "sm_mhz": clk.get("sm_mhz"),
+                     "note": "CUDA events around each sdv2_rope_append_kv call inside the step; the call's "
+                             "43 MB of writes may still sit in L2 when its end event is recorded (the next "
+                             "attention launch reads them from there)"}
 
     res = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": dist.world,
            "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms_max / args.steps, 3),
@@ -448,12 +568,23 @@ def run_ours(args, dist):
            "latent_frames_per_s": round(latent_fps, 3),
            "pct_bf16_peak": round(100.0 * value / peak, 2),
            "gpu_launches": launches_per_step * args.steps,
-           "clocks": clk, "roofline": roofline, "e2e": e2e, "impl": "ours"}
+           "clocks": clk, "roofline": roofline, "roofline_rope_append": roofline_rope, "e2e": e2e,
+           "impl": "ours"}
+    motion_np = frames.cpu().numpy() if dist.world == 1 and not args.no_cpu_baseline else None
+    state.close()
+    del cfg, sess, qkv, outs, frames, ssd, mrms
+    if not args.no_workloads:
+        others = [n for n in ("wan13b_720p", "wan14b_480p", "stream_batch") if n != args.workload]
+        res["workloads"] = {n: measure_other_workload(n, args.workload_steps, 3, dist, dev, stream,
+                                                      0 if args.no_cpu_baseline else 2.5) for n in others}
+    res["_motion_frames"] = motion_np
     return res
 
 
-def cpu_baseline_entry(w, seconds=12.0, single_seconds=4.0):
-    """The oracle on all host cores (the reported value) and, for scale, on one thread."""
+def cpu_baseline_entry(w, motion_np, seconds=10.0, single_seconds=3.0, rope_seconds=2.0, motion_seconds=1.5):
+    """The oracle on all host cores (the reported value) and, for scale, on one thread: the
+    attention on sampled rows, plus the Causal-RoPE + append of whole chunks and the motion SSD
+    of the step's frames."""
     import oracle
     flops, secs, rows, threads = oracle_sample(w, seconds)
     all_threads = oracle.num_threads()
@@ -462,12 +593,33 @@ def cpu_baseline_entry(w, seconds=12.0, single_seconds=4.0):
         f1, s1, r1, _ = oracle_sample(w, single_seconds, seed=1, max_rows=256)
     finally:
         oracle.set_num_threads(all_threads)
-    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "single_thread_value": round(f1 / s1 / 1e12, 7),
-            "sample": "fp64 oracle attention of %d query rows against the steady-state %d keys of one head "
-                      "(bf16 inputs), %.1f s on %d threads; single_thread_value: %d rows, %.1f s on 1 thread; "
-                      "TFLOP/s counts the same 4*D*Nkv flops per row as the GPU metric"
-                      % (rows, w.slots * w.hw, secs, threads, r1, s1)}
+    out = {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "single_thread_value": round(f1 / s1 / 1e12, 7),
+           "sample": "fp64 oracle attention of %d query rows against the steady-state %d keys of one head "
+                     "(bf16 inputs), %.1f s on %d threads; single_thread_value: %d rows, %.1f s on 1 thread; "
+                     "TFLOP/s counts the same 4*D*Nkv flops per row as the GPU metric"
+                     % (rows, w.slots * w.hw, secs, threads, r1, s1)}
+
+    def both(fn, unit_scale, unit, what):
+        n, t, per = fn()
+        oracle.set_num_threads(1)
+        try:
+            n1, t1, _ = fn()
+        finally:
+            oracle.set_num_threads(all_threads)
+        return {"value": round(n * per / t / unit_scale, 4), "unit": unit, "cores": all_threads,
+                "single_thread_value": round(n1 * per / t1 / unit_scale, 5), "kind": "oracle",
+                "sample": "%s: %d passes in %.2f s on %d threads; %d in %.2f s on 1 thread"
+                          % (what, n, t, all_threads, n1, t1)}
+    out["rope_append"] = both(lambda: oracle_rope_append_sample(w, rope_seconds), 1e9, "GB/s",
+                              "rope_spec of the chunk's q and k (%d tokens x %d heads) + FrameListCache.append "
+                              "of its %d frames; GB/s counts the kernel's 1536 algorithmic bytes per token-head"
+                              % (w.nq, w.heads, w.chunk_frames))
+    if motion_np is not None:
+        out["motion"] = both(lambda: oracle_motion_sample(motion_np, motion_seconds), 1e9, "GB/s",
+                             "motion_ssd of the step's %d frames of %s per stream (exact uint64), GB/s of "
+                             "frame bytes read" % (motion_np.shape[1], "x".join(map(str, motion_np.shape[2:]))))
+    return out
 
 
 def run_reference(args, dist):
@@ -506,6 +658,9 @@ def main():
     ap.add_argument("--workload", default="wan13b_480p", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the steady-state lines of the other workloads (1.3B-720p, 14B-480p, stream batch)")
+    ap.add_argument("--workload-steps", type=int, default=3, help="timed steps of each other workload")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the workload's layer count (profiling runs only; 0 = workload's)")
     args = ap.parse_args()
@@ -522,9 +677,10 @@ def main():
 
     dist = Dist(args.gpus)
     res = run_ours(args, dist)
+    motion_np = res.pop("_motion_frames", None)
     if dist.rank == 0:
         if dist.world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline_entry(WORKLOADS[args.workload])
+            res["cpu_baseline"] = cpu_baseline_entry(WORKLOADS[args.workload], motion_np)
         print(json.dumps(res), flush=True)
     dist.close()
     return 0

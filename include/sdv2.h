@@ -15,7 +15,8 @@
  *    before the call returns.
  *  - Work is enqueued asynchronously on the caller's CUDA stream (`stream`, a cudaStream_t
  *    passed as void*; NULL = the legacy default stream).  No entry point synchronizes, except
- *    sdv2_workspace_init and sdv2_check_device_error, which say so.
+ *    sdv2_workspace_init, sdv2_check_device_error and sdv2_noalloc_check_device_error, which
+ *    say so.
  *  - Arguments are validated on the host before anything is launched; a rejected call
  *    launches nothing and returns SDV2_ERR_INVALID_ARG or SDV2_ERR_UNSUPPORTED.  A failed
  *    launch returns SDV2_ERR_CUDA.  sdv2_last_error() gives a one-line reason (per thread).
@@ -126,8 +127,8 @@ sdv2_status sdv2_cache_reset(const sdv2_stream_cfg* cfg, void* k_cache, void* v_
 /*
  * Causal-RoPE + cache append for chunk chunk_index[b] of every stream b.
  *
- * start_frame, chunk_index: HOST arrays of B int64 (>= 0): the global start frame S_b of
- *   stream b and the chunk being appended.  Positions are derived as in the struct comment.
+ * start_frame, chunk_index: HOST arrays of B int64, start_frame in [0, 2^50] and chunk_index in
+ *   [0, 2^40]: the global start frame S_b of stream b and the chunk being appended.  Positions are derived as in the struct comment.
  * q, k, v: device bf16, token-major [B][Nq][H][D], with qkv_token_stride elements between
  *   consecutive tokens (so a packed [token][3][H][D] projection output can be passed as three
  *   pointers) and Nq*stride elements between streams.
@@ -178,7 +179,7 @@ sdv2_status sdv2_qkv_rope_append(const sdv2_stream_cfg* cfg, const int64_t* star
  * There is no mask inside the valid rows: the chunk attends to itself in full and to every
  * retained earlier frame (chunk-causal attention of a Self-Forcing-style streaming DiT).
  *
- * chunk_index: HOST array of B int64 (>= 0).
+ * chunk_index: HOST array of B int64 in [0, 2^40].
  * q_rot: device bf16 [B][H][Nq][D]; k_cache, v_cache: device bf16 [B][H][(F_s+W)*HW][D].
  * scale: softmax scale; <= 0 selects 1/sqrt(D).
  * out: device bf16 [B][Nq][H][D] (token-major, ready for the output projection).
@@ -212,21 +213,34 @@ sdv2_status sdv2_chunk_attention(const sdv2_stream_cfg* cfg, const int64_t* chun
  * - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
  *   with that device current) and keeps it; make that first call before any stream capture.
  * - Every call on a device shares the array, which keeps the previous call's contents; each
- *   call clears the error word and counters on `stream` (a memset) before its kernel.  Calls
- *   whose work overlaps on the GPU (other streams, graph branches) race on the array: do not
+ *   call clears the key-split counters on `stream` (a memset) before its kernel.  Calls whose
+ *   work overlaps on the GPU (other streams, graph branches) race on the array: do not
  *   overlap them.
- * - Key splits are chosen as for sdv2_chunk_attention, then reduced until their partial rows
- *   fit in the array (results stay within the same tolerance; speed may differ).
+ * - Key splits are chosen as for sdv2_chunk_attention (sdv2_debug_set_kv_splits applies here
+ *   too), then reduced until their partial rows fit in the array (results stay within the same
+ *   tolerance; speed may differ).  sdv2_last_kv_splits reports the count used.
  * - Sizes beyond the array's reach are rejected with SDV2_ERR_UNSUPPORTED before anything is
- *   enqueued: batch * heads * ceil(Nq / 256) must be <= 16384.  Bounded device waits use the
- *   default 2 s limit; a timeout leaves the outputs undefined and is not reported here (use
- *   sdv2_chunk_attention with a workspace and sdv2_check_device_error to observe it).
+ *   enqueued: batch * heads * ceil(Nq / 256) must be <= 16384.
+ * - Bounded device waits use the limit of sdv2_set_wait_timeout_ns.  A wait that gives up
+ *   leaves this call's outputs undefined and sets the array's error word, which later calls
+ *   do not clear: sdv2_noalloc_check_device_error reports it (and clears it).
  * Other arguments, layouts and numerics: as sdv2_chunk_attention.
  */
 sdv2_status sdv2_chunk_attention_noalloc(const sdv2_stream_cfg* cfg, const int64_t* chunk_index,
                                          const void* q_rot, const void* k_cache,
                                          const void* v_cache, float scale, void* out, float* lse,
                                          void* stream);
+
+/*
+ * Error check of sdv2_chunk_attention_noalloc on the current device, allocation-free as well
+ * (the pages have no counterpart).  Synchronizes `stream`, reads the static array's error word
+ * with one cudaMemcpyAsync and returns SDV2_ERR_TIMEOUT if a bounded device wait of an earlier
+ * sdv2_chunk_attention_noalloc call gave up since the last check (that call's outputs are
+ * undefined), SDV2_ERR_CUDA on a CUDA error, else SDV2_OK.  After a timeout it clears the
+ * error word and the key-split counters, so the next call starts clean.  Calls on the device
+ * that are still running on other streams must be finished first (they share the array).
+ */
+sdv2_status sdv2_noalloc_check_device_error(void* stream);
 
 /*
  * Motion magnitude of adjacent frames ("StreamDiffusionV2" review page, section 二 table and

@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     lib_path,
     meta_bytes,
     motion_l2,
+    noalloc_check_device_error,
     noise_from_motion,
     qkv_rope_append,
     rope_append_kv,

@@ -13,7 +13,7 @@ STATUS_NAMES = {0: "SDV2_OK", 1: "SDV2_ERR_INVALID_ARG", 2: "SDV2_ERR_UNSUPPORTE
 # Every symbol that include/sdv2.h declares.
 EXPORTS = ["sdv2_workspace_bytes", "sdv2_cache_bytes", "sdv2_meta_bytes", "sdv2_visible_tokens",
            "sdv2_workspace_init", "sdv2_cache_reset", "sdv2_rope_append_kv", "sdv2_qkv_rope_append", "sdv2_chunk_attention",
-           "sdv2_chunk_attention_noalloc",
+           "sdv2_chunk_attention_noalloc", "sdv2_noalloc_check_device_error",
            "sdv2_motion_l2", "sdv2_rope_refresh_rerotate", "sdv2_sink_update", "sdv2_noise_from_motion",
            "sdv2_check_device_error", "sdv2_set_wait_timeout_ns",
            "sdv2_debug_drop_kv_tile", "sdv2_debug_set_kv_splits", "sdv2_last_kv_splits",
@@ -93,6 +93,8 @@ def lib():
         L.sdv2_chunk_attention.argtypes = [cfgp, i64p, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
         L.sdv2_chunk_attention_noalloc.restype = ctypes.c_int
         L.sdv2_chunk_attention_noalloc.argtypes = [cfgp, i64p, vp, vp, vp, ctypes.c_float, vp, vp, vp]
+        L.sdv2_noalloc_check_device_error.restype = ctypes.c_int
+        L.sdv2_noalloc_check_device_error.argtypes = [vp]
         L.sdv2_motion_l2.restype = ctypes.c_int
         L.sdv2_motion_l2.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp, vp]
         L.sdv2_rope_refresh_rerotate.restype = ctypes.c_int
@@ -249,6 +251,11 @@ def chunk_attention_noalloc(cfg, chunk_index, q_rot, k_cache, v_cache, out, lse=
                                               _dev(q_rot, "q_rot", qo), _dev(k_cache, "k_cache", cb),
                                               _dev(v_cache, "v_cache", cb), float(scale), _dev(out, "out", qo),
                                               _dev(lse, "lse", lb), _stream(stream)), "sdv2_chunk_attention_noalloc")
+
+
+def noalloc_check_device_error(stream=None):
+    """sdv2_noalloc_check_device_error: raises SDV2Error (status 4) after a timed-out no-alloc call."""
+    _check(lib().sdv2_noalloc_check_device_error(_stream(stream)), "sdv2_noalloc_check_device_error")
 
 
 def motion_l2(frames, ssd, m=None, stream=None):

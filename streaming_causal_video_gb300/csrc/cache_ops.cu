@@ -96,12 +96,12 @@ __global__ void __launch_bounds__(256) sink_update_kernel(const __grid_constant_
     const uint4* vf = reinterpret_cast<const uint4*>(p.v_cache) + (head_base + static_cast<int64_t>(src) * p.HW) * 16;
     uint4* kt = reinterpret_cast<uint4*>(p.k_cache) + (head_base + static_cast<int64_t>(s) * p.HW) * 16;
     uint4* vt = reinterpret_cast<uint4*>(p.v_cache) + (head_base + static_cast<int64_t>(s) * p.HW) * 16;
-    const int n = p.HW * 16;
-    const int i0 = blockIdx.x * (256 * kSinkVecsPerThread) + threadIdx.x;
+    const int64_t n = static_cast<int64_t>(p.HW) * 16;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * (256 * kSinkVecsPerThread) + threadIdx.x;
     uint4 kv[kSinkVecsPerThread], vv[kSinkVecsPerThread];
 #pragma unroll
     for (int u = 0; u < kSinkVecsPerThread; ++u) {
-        const int i = i0 + u * 256;
+        const int64_t i = i0 + u * 256;
         if (i < n) {
             kv[u] = kf[i];
             vv[u] = vf[i];
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(256) sink_update_kernel(const __grid_constant_
     }
 #pragma unroll
     for (int u = 0; u < kSinkVecsPerThread; ++u) {
-        const int i = i0 + u * 256;
+        const int64_t i = i0 + u * 256;
         if (i < n) {
             kt[i] = kv[u];
             vt[i] = vv[u];
@@ -171,7 +171,7 @@ cudaError_t launch_sink_update(const SinkUpdateParams& p, cudaStream_t s)
 {
     if (p.B == 0 || p.Fs == 0 || p.HW == 0 || p.H == 0) return cudaSuccess;
     const int per_block = 256 * kSinkVecsPerThread;
-    const dim3 grid(static_cast<unsigned>((p.HW * 16 + per_block - 1) / per_block), static_cast<unsigned>(p.H),
+    const dim3 grid(static_cast<unsigned>((static_cast<int64_t>(p.HW) * 16 + per_block - 1) / per_block), static_cast<unsigned>(p.H),
                     static_cast<unsigned>(p.B * p.Fs));
     sink_update_kernel<<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();

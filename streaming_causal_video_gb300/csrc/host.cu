@@ -140,7 +140,7 @@ sdv2_status check_append_args(const sdv2_stream_cfg* c, const int64_t* start_fra
     for (int b = 0; b < B; ++b) {
         if (start_frame[b] < 0 || chunk_index[b] < 0)
             return fail(SDV2_ERR_INVALID_ARG, "start_frame[%d] and chunk_index[%d] must be >= 0", b, b);
-        if (chunk_index[b] > (int64_t(1) << 40) || start_frame[b] > (int64_t(1) << 50))
+        if (chunk_index[b] > sdv2::kMaxChunkIndex || start_frame[b] > (int64_t(1) << 50))
             return fail(SDV2_ERR_INVALID_ARG, "start_frame[%d] or chunk_index[%d] too large", b, b);
     }
     return SDV2_OK;
@@ -207,6 +207,10 @@ thread_local int g_last_splits = 0;
 
 namespace sdv2 {
 void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg ? msg : ""); }
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+int64_t debug_drop_tile() { return g_drop_tile.load(); }
+int debug_force_splits() { return g_force_splits.load(); }
+void set_last_kv_splits(int splits) { g_last_splits = splits; }
 }  // namespace sdv2
 
 extern "C" {
@@ -355,7 +359,8 @@ sdv2_status sdv2_chunk_attention(const sdv2_stream_cfg* c, const int64_t* chunk_
     if (!std::isfinite(scale)) return fail(SDV2_ERR_INVALID_ARG, "scale must be finite");
     int32_t nkv[sdv2::kMaxAttnStreams];
     for (int b = 0; b < c->batch; ++b) {
-        if (chunk_index[b] < 0) return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be >= 0", b);
+        if (chunk_index[b] < 0 || chunk_index[b] > sdv2::kMaxChunkIndex)
+            return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be in [0, 2^40]", b);
         nkv[b] = static_cast<int32_t>(visible_frames(c, chunk_index[b]) * hw_of(c));
     }
     if ((s = check_device()) != SDV2_OK) return s;
@@ -448,7 +453,8 @@ sdv2_status sdv2_rope_refresh_rerotate(const sdv2_stream_cfg* c, const int64_t* 
     if (c->batch > sdv2::kMaxCacheStreams) return fail(SDV2_ERR_UNSUPPORTED, "more than 64 streams");
     if (c->rope_t / 2 > sdv2::kMaxTimePairsPerAxis) return fail(SDV2_ERR_UNSUPPORTED, "rope_t > 128");
     for (int b = 0; b < c->batch; ++b)
-        if (chunk_index[b] < 0) return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be >= 0", b);
+        if (chunk_index[b] < 0 || chunk_index[b] > sdv2::kMaxChunkIndex)
+            return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be in [0, 2^40]", b);
     if ((s = check_device()) != SDV2_OK) return s;
     sdv2::RerotateParams p{};
     p.k_cache = static_cast<uint16_t*>(k_cache);
@@ -498,7 +504,8 @@ sdv2_status sdv2_sink_update(const sdv2_stream_cfg* c, const int64_t* chunk_inde
     p.nslots = static_cast<int32_t>(slots_of(c));
     bool any = false;
     for (int b = 0; b < c->batch; ++b) {
-        if (chunk_index[b] < 0) return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be >= 0", b);
+        if (chunk_index[b] < 0 || chunk_index[b] > sdv2::kMaxChunkIndex)
+            return fail(SDV2_ERR_INVALID_ARG, "chunk_index[%d] must be in [0, 2^40]", b);
         p.active[b] = update[b] ? 1 : 0;
         if (!p.active[b]) continue;
         const int64_t n = (chunk_index[b] + 1) * c->chunk_frames;   // frames appended so far

@@ -164,6 +164,17 @@ cudaError_t launch_qkv_rope(QkvRopeParams& p, const void* x, const void* w, int6
 // Sets the per-thread message returned by sdv2_last_error().
 void set_last_error(const char* msg);
 
+// Process-wide settings of the attention entry points (sdv2_set_wait_timeout_ns,
+// sdv2_debug_drop_kv_tile, sdv2_debug_set_kv_splits) and the per-thread split count that
+// sdv2_last_kv_splits reports.
+uint64_t wait_timeout_ns();
+int64_t debug_drop_tile();
+int debug_force_splits();
+void set_last_kv_splits(int splits);
+
+// Largest chunk index the entry points accept (frame numbers c*F stay far inside int64).
+constexpr int64_t kMaxChunkIndex = int64_t(1) << 40;
+
 // ---- misc kernels -----------------------------------------------------------------------------
 
 cudaError_t launch_cache_reset(uint16_t* k, uint16_t* v, size_t cache_bytes, sdv2_slot_meta* meta,

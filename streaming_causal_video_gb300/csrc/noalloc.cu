@@ -9,9 +9,11 @@
 //
 // The array is part of the library's module: every GPU that loads the library holds its
 // kNoAllocScratchBytes until the process exits.  All calls on a device share it, and it keeps
-// the previous call's contents; each call therefore clears the error word and the counters on
-// its stream before the kernel runs.  Calls whose kernels overlap on the GPU (different
-// streams, or graph branches) race on the array and must not be issued.
+// the previous call's contents; each call therefore clears the split counters on its stream
+// before the kernel runs.  The error word is not cleared by a call: a bounded wait that gave up
+// leaves it set until sdv2_noalloc_check_device_error reads it, so a later call cannot hide an
+// earlier timeout.  Calls whose kernels overlap on the GPU (different streams, or graph
+// branches) race on the array and must not be issued.
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -39,6 +41,30 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 std::mutex g_na_mutex;
 unsigned char* g_na_ptr[64] = {};          // device address of the array, per device
+
+// Device address of the array on the current device `dev`, looked up (with that device
+// current) on the first call and kept.  The first lookup also clears the error word and the
+// counters on `st`.  Returns null if the lookup failed.
+unsigned char* scratch_base(int dev, cudaStream_t st, cudaError_t* err)
+{
+    std::lock_guard<std::mutex> lock(g_na_mutex);
+    *err = cudaSuccess;
+    if (!g_na_ptr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            *err = e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+            return nullptr;
+        }
+        e = cudaMemsetAsync(p, 0, kNaPartMl, st);
+        if (e != cudaSuccess) {
+            *err = e;
+            return nullptr;
+        }
+        g_na_ptr[dev] = static_cast<unsigned char*>(p);
+    }
+    return g_na_ptr[dev];
+}
 
 sdv2_status na_fail(sdv2_status s, const char* msg)
 {
@@ -77,7 +103,8 @@ extern "C" sdv2_status sdv2_chunk_attention_noalloc(const sdv2_stream_cfg* cfg, 
     int32_t nkv[kMaxAttnStreams];
     int min_tiles = 1 << 30;
     for (int b = 0; b < cfg->batch; ++b) {
-        if (chunk_index[b] < 0) return na_fail(SDV2_ERR_INVALID_ARG, "chunk_index must be >= 0");
+        if (chunk_index[b] < 0 || chunk_index[b] > kMaxChunkIndex)
+            return na_fail(SDV2_ERR_INVALID_ARG, "chunk_index must be in [0, 2^40]");
         nkv[b] = static_cast<int32_t>(sdv2_visible_tokens(cfg, chunk_index[b]));
         min_tiles = std::min(min_tiles, (nkv[b] + 127) / 128);
     }
@@ -91,26 +118,21 @@ extern "C" sdv2_status sdv2_chunk_attention_noalloc(const sdv2_stream_cfg* cfg, 
     if (major != 10 || minor != 3) return na_fail(SDV2_ERR_UNSUPPORTED, "the library is built for sm_103a (GB300) only");
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
 
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     // Set-up, once per device and with that device current: the device address of the array.
-    unsigned char* base;
-    {
-        std::lock_guard<std::mutex> lock(g_na_mutex);
-        if (!g_na_ptr[dev]) {
-            void* p = nullptr;
-            cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-            if (e != cudaSuccess || !p) return na_fail(SDV2_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
-            g_na_ptr[dev] = static_cast<unsigned char*>(p);
-        }
-        base = g_na_ptr[dev];
-    }
+    cudaError_t e = cudaSuccess;
+    unsigned char* base = scratch_base(dev, st, &e);
+    if (!base) return na_fail(SDV2_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
 
-    // Key splits: the automatic choice, reduced until its partial rows fit in the array.
-    int splits = choose_kv_splits(items, min_tiles, std::max(1, sms));
+    // Key splits: the automatic (or forced) choice, reduced until its partial rows fit in the array.
+    const int force = debug_force_splits();
+    int splits = force > 0 ? std::min(force, std::min(kMaxKvSplits, min_tiles))
+                           : choose_kv_splits(items, min_tiles, std::max(1, sms));
     while (splits > 1 && items * splits * kAttnRowsPerCta > kNaRows) --splits;
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents: clear the error word and the counters.
-    cudaError_t e = cudaMemsetAsync(base, 0, kNaPartMl, st);
+    // The array keeps the previous call's contents: clear the split counters (the error word
+    // stays, see above).
+    e = cudaMemsetAsync(base + kNaCounters, 0, kNaCountersBytes, st);
     if (e != cudaSuccess) return na_fail(SDV2_ERR_CUDA, "clearing the static scratch failed");
     AttnScratch scratch{reinterpret_cast<uint32_t*>(base), reinterpret_cast<int32_t*>(base + kNaCounters),
                         reinterpret_cast<float*>(base + kNaPartMl), reinterpret_cast<float*>(base + kNaPartO)};
@@ -119,8 +141,37 @@ extern "C" sdv2_status sdv2_chunk_attention_noalloc(const sdv2_stream_cfg* cfg, 
     e = launch_chunk_attention(static_cast<const uint16_t*>(q_rot), static_cast<const uint16_t*>(k_cache),
                                static_cast<const uint16_t*>(v_cache), cfg->batch, cfg->heads, nq,
                                (static_cast<int64_t>(cfg->sink_frames) + cfg->window_frames) * hw, nkv, scale,
-                               static_cast<uint16_t*>(out), lse, scratch, 2000000000ull, -1, splits, st, &used, &why);
+                               static_cast<uint16_t*>(out), lse, scratch, wait_timeout_ns(), debug_drop_tile(), splits,
+                               st, &used, &why);
     if (e != cudaSuccess) return na_fail(SDV2_ERR_CUDA, why);
+    set_last_kv_splits(used);
+    set_last_error("");
+    return SDV2_OK;
+}
+
+extern "C" sdv2_status sdv2_noalloc_check_device_error(void* stream)
+{
+    using namespace sdv2;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return na_fail(SDV2_ERR_CUDA, "cudaGetDevice failed");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    unsigned char* base = scratch_base(dev, st, &e);
+    if (!base) return na_fail(SDV2_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+    uint32_t word = 0;
+    e = cudaMemcpyAsync(&word, base, sizeof(word), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess && word) {
+        // clear the error word and the counters an aborted launch may have left mid-count
+        e = cudaMemsetAsync(base, 0, kNaPartMl, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    if (e != cudaSuccess) {
+        char buf[200];
+        snprintf(buf, sizeof(buf), "reading the static scratch's error word: %s", cudaGetErrorString(e));
+        return na_fail(SDV2_ERR_CUDA, buf);
+    }
+    if (word & kErrTimeout) return na_fail(SDV2_ERR_TIMEOUT, "a bounded device wait gave up");
     set_last_error("");
     return SDV2_OK;
 }

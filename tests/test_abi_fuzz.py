@@ -85,3 +85,29 @@ def test_random_configs_with_one_broken_field_are_rejected(field, value):
                 fn(c, *args)
             assert e.value.status in (1, 2), (field, value, e.value.status)
             assert sd.lib().sdv2_last_error(), (field, value)
+
+
+@pytest.mark.parametrize("chunk", [-1, (1 << 40) + 1, (1 << 62)])
+@pytest.mark.parametrize("name,batch", [("tiny", 1), ("tiny", 3), ("stream_batch", 4)])
+def test_chunk_index_outside_zero_to_two_pow_40_is_rejected_everywhere(chunk, name, batch):
+    """Every entry point that takes chunk indices refuses one outside [0, 2^40] before anything
+    is enqueued (frame numbers c*F and the visible-prefix arithmetic stay far inside int64)."""
+    import ctypes
+    c = sd.StreamConfig.make(**stream_config_dict(WORKLOADS[name], batch=batch))
+    L = sd.lib()
+    for bad in range(batch):
+        idx = [5] * batch
+        idx[bad] = chunk
+        arr = (ctypes.c_int64 * batch)(*idx)
+        zeros = (ctypes.c_int64 * batch)(*([0] * batch))
+        upd = (ctypes.c_int32 * batch)(*([1] * batch))
+        calls = [
+            lambda: L.sdv2_rope_append_kv(ctypes.byref(c), zeros, arr, *([FAKE] * 8), None),
+            lambda: L.sdv2_chunk_attention(ctypes.byref(c), arr, FAKE, FAKE, FAKE, 0.0, FAKE, None, FAKE, None),
+            lambda: L.sdv2_chunk_attention_noalloc(ctypes.byref(c), arr, FAKE, FAKE, FAKE, 0.0, FAKE, None, None),
+            lambda: L.sdv2_rope_refresh_rerotate(ctypes.byref(c), arr, FAKE, FAKE, None),
+            lambda: L.sdv2_sink_update(ctypes.byref(c), arr, upd, FAKE, FAKE, FAKE, None),
+        ]
+        for k, call in enumerate(calls):
+            assert call() == 1, k
+            assert b"chunk_index" in L.sdv2_last_error(), (k, L.sdv2_last_error())

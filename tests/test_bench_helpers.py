@@ -5,6 +5,8 @@ import json
 import os
 import threading
 
+import pytest
+
 import bench
 
 CSRC = os.path.join(bench.ROOT, "streaming_causal_video_gb300", "csrc")
@@ -105,7 +107,10 @@ def test_traffic_record_differs_from_its_capture_only_in_the_encoder_lookup():
     with open(path) as fh:
         rec = json.load(fh)
     if "captured_source_hash" not in rec:
-        return
+        pytest.skip("the traffic record carries no captured_source_hash: it was captured on the sources it names")
+    if rec["source_hash"] != bench.attention_source_hash():
+        assert bench.profiled_traffic("wan13b_480p") is None
+        pytest.skip("the traffic record predates the current attention source: the bench reports traffic null")
     start_tag = "EncodeTiledFn get_encode_tiled()"
 
     def captured(f):
@@ -117,3 +122,20 @@ def test_traffic_record_differs_from_its_capture_only_in_the_encoder_lookup():
         return text[:a] + _CAPTURED_GET_ENCODE_TILED + text[b:]
     assert bench.attention_source_hash(captured) == rec["captured_source_hash"]
     assert bench.attention_source_hash() == rec["source_hash"]
+
+
+def test_cpu_baseline_entry_times_attention_rope_append_and_motion():
+    """The bench's CPU-baseline leg on the tiny workload with short samples: all three parts of
+    the path are timed on all cores and on one thread, with their units and core counts."""
+    from synth_inputs import WORKLOADS, motion_frames_host
+    w = WORKLOADS["tiny"]
+    frames = motion_frames_host(1, 5, 16, 32, 3, seed=2).numpy()
+    out = bench.cpu_baseline_entry(w, frames, seconds=0.2, single_seconds=0.1, rope_seconds=0.1,
+                                   motion_seconds=0.05)
+    assert out["kind"] == "oracle" and out["value"] > 0 and out["single_thread_value"] > 0
+    for part in ("rope_append", "motion"):
+        d = out[part]
+        assert d["unit"] == "GB/s" and d["value"] > 0 and d["single_thread_value"] > 0
+        assert d["cores"] >= 1 and d["kind"] == "oracle"
+    assert "motion" not in bench.cpu_baseline_entry(w, None, seconds=0.1, single_seconds=0.05,
+                                                    rope_seconds=0.05)

@@ -302,11 +302,44 @@ def test_stream_batch_full_shape_identical_streams_shift_invariance():
     for c in range(3):
         q_rot_o = ls.step([c] * 4, same_streams=True)
         ls.check_q_rot(q_rot_o)
+        ls.check_cache()
         ls.check_attention(q_rot_o, rows=rows, heads=[0, 7])
     out = to_f64(ls.sess.out)
     for b in range(1, 4):
         err = np.abs(out[b] - out[0])
         assert err.max() <= 2 * MAX_ABS and err.mean() <= 2 * MEAN_ABS
+
+
+@pytest.mark.parametrize("rerotate", [False, True])
+def test_stream_batch_full_shape_through_the_first_refresh(rerotate):
+    """The stream-batch workload at its own shape (4 streams, 12 heads, 30x52 tokens per frame,
+    chunks of 3 frames, sink 3 + window 18, RoPE refresh every 64 chunks, start offsets 0, 1e3,
+    1e4, 1e5), one layer streamed through chunks 0-66: the first chunks, the first window wrap and
+    the chunks around the refresh at 64 are checked -- q_rot, every retained frame's K/V rows and
+    all slot metadata bit-exact, attention on sampled rows of two heads.  With rerotate the
+    window keys are turned back by F*R at the refresh chunk (second reading of the refresh)
+    before its first append, on both sides."""
+    w = WORKLOADS["stream_batch"]
+    ls = LockStep(w)
+    L = ls.sess.layers[0]
+    check = {0, 6, 7, 62, 63, 64, 65, 66}
+    for c in range(67):
+        if rerotate:
+            sd.rope_refresh_rerotate(ls.cfg, [c] * w.batch, L.k, L.meta)
+            torch.cuda.synchronize()
+            refresh = [o.refresh_rerotate(c) for o in ls.oracles]
+            assert all(refresh) == (c == 64) and any(refresh) == (c == 64)
+        q_rot_o = ls.step([c] * w.batch)
+        if c in check:
+            ls.check_q_rot(q_rot_o)
+            ls.check_cache()
+            ls.check_attention(q_rot_o, rows=sample_rows(w.nq, 20, 300 + c), heads=[0, 11])
+            if c == 64:
+                meta = L.meta.cpu().numpy()
+                for b, s0 in enumerate(w.start_frames):
+                    # the new chunk's frames restart at the stream's own start frame
+                    assert {int(meta[b, oracle.slot_of_frame(64 * 3 + i, 3, 18), 1]) for i in range(3)} == \
+                        {s0, s0 + 1, s0 + 2}
 
 
 # ------------------------------------------------------------------------------------------
