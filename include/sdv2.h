@@ -335,12 +335,6 @@ void sdv2_debug_set_kv_splits(int32_t splits);
 /* Split count used by this thread's most recent sdv2_chunk_attention call. */
 int32_t sdv2_last_kv_splits(void);
 
-/* The attention softmax's two ways of computing 2^x, side by side, for tests: y_fma[i] from the
- * FMA-pipe polynomial (range reduction x = floor(x) + f, minimax cubic for 2^f; relative error
- * <= 7.5e-5 on [-125, 8]) used for one score pair in four, y_mufu[i] from ex2.approx.ftz.f32
- * used for the others.  x, y_fma, y_mufu: device fp32 [n], n even. */
-sdv2_status sdv2_debug_exp2(const float* x, float* y_fma, float* y_mufu, int64_t n, void* stream);
-
 const char* sdv2_status_string(sdv2_status s);
 const char* sdv2_last_error(void);
 

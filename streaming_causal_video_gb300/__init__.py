@@ -15,7 +15,6 @@ from ._binding import (  # noqa: F401
     chunk_attention,
     chunk_attention_noalloc,
     debug_drop_kv_tile,
-    debug_exp2,
     debug_set_kv_splits,
     last_kv_splits,
     exported_symbols,

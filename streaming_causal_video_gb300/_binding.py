@@ -16,7 +16,7 @@ EXPORTS = ["sdv2_workspace_bytes", "sdv2_cache_bytes", "sdv2_meta_bytes", "sdv2_
            "sdv2_chunk_attention_noalloc", "sdv2_noalloc_check_device_error",
            "sdv2_motion_l2", "sdv2_rope_refresh_rerotate", "sdv2_sink_update", "sdv2_noise_from_motion",
            "sdv2_check_device_error", "sdv2_set_wait_timeout_ns",
-           "sdv2_debug_drop_kv_tile", "sdv2_debug_set_kv_splits", "sdv2_last_kv_splits", "sdv2_debug_exp2",
+           "sdv2_debug_drop_kv_tile", "sdv2_debug_set_kv_splits", "sdv2_last_kv_splits",
            "sdv2_status_string", "sdv2_last_error"]
 
 
@@ -113,8 +113,6 @@ def lib():
         L.sdv2_debug_set_kv_splits.argtypes = [i32]
         L.sdv2_last_kv_splits.restype = i32
         L.sdv2_last_kv_splits.argtypes = []
-        L.sdv2_debug_exp2.restype = ctypes.c_int
-        L.sdv2_debug_exp2.argtypes = [vp, vp, vp, i64, vp]
         L.sdv2_status_string.restype = ctypes.c_char_p
         L.sdv2_status_string.argtypes = [ctypes.c_int]
         L.sdv2_last_error.restype = ctypes.c_char_p
@@ -306,13 +304,6 @@ def debug_drop_kv_tile(tile: int):
 
 def debug_set_kv_splits(n: int):
     lib().sdv2_debug_set_kv_splits(int(n))
-
-
-def debug_exp2(x, y_fma, y_mufu, stream=None):
-    """sdv2_debug_exp2 on device fp32 tensors of the same even length."""
-    n = x.numel()
-    _check(lib().sdv2_debug_exp2(_dev(x, "x", n * 4), _dev(y_fma, "y_fma", n * 4), _dev(y_mufu, "y_mufu", n * 4),
-                                 n, _stream(stream)), "sdv2_debug_exp2")
 
 
 def last_kv_splits() -> int:

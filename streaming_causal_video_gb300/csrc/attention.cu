@@ -68,7 +68,6 @@ constexpr int NTHREADS = (4 * NQT + 3) * 32;
 constexpr int PREFETCH_TILES = 4;        // K/V tiles prefetched into L2 ahead of their load
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-constexpr int kFmaExpEvery = 4;             // one score pair in kFmaExpEvery exponentiated on the FMA pipe
 constexpr float kLn2 = 0.6931471805599453f;
 
 // barrier indices
@@ -337,11 +336,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                     m_run = m_new;
                 }
             }
-            // p = 2^(s * scale * log2(e) - m): one packed FFMA per two scores, then 2^x on the
-            // MUFU unit (ex2.approx) for three pairs in four and on the FMA pipe (exp2_fma_x2)
-            // for the fourth: with every exponential on MUFU, MUFU alone needs as many cycles
-            // per key tile as the tensor core; the row sum accumulates pairs with packed adds in
-            // 4 independent chains.
+            // p = 2^(s * scale * log2(e) - m): one packed FFMA per two scores, one MUFU.EX2 per
+            // score; the row sum accumulates pairs with packed adds in 4 independent chains.
             const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
             const uint64_t negm2 = f32x2_pack(-m_run, -m_run);
             uint64_t sum4[4];
@@ -354,15 +350,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                 for (int i = 0; i < 32; ++i) {
                     const int e = hf * 64 + 2 * i;
                     const uint64_t x = ffma2(f32x2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sl2x2, negm2);
-                    float p0, p1;
-                    if ((i % kFmaExpEvery) == kFmaExpEvery - 1) {
-                        exp2_fma_x2(x, p0, p1);
-                    } else {
-                        float x0, x1;
-                        f32x2_unpack(x, x0, x1);
-                        p0 = ex2_approx(x0);
-                        p1 = ex2_approx(x1);
-                    }
+                    float x0, x1;
+                    f32x2_unpack(x, x0, x1);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
                     sum4[i & 3] = fadd2(sum4[i & 3], f32x2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
@@ -543,20 +534,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
 #undef BAR
 }
 
-// The two exponentials of the softmax side by side, for tests: y_fma[i] from exp2_fma_x2,
-// y_mufu[i] from ex2.approx; n even.
-__global__ void exp2_check_kernel(const float* __restrict__ x, float* __restrict__ y_fma,
-                                  float* __restrict__ y_mufu, int64_t npairs)
-{
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= npairs) return;
-    const float2 v = reinterpret_cast<const float2*>(x)[i];
-    float a, b;
-    exp2_fma_x2(f32x2_pack(v.x, v.y), a, b);
-    reinterpret_cast<float2*>(y_fma)[i] = make_float2(a, b);
-    reinterpret_cast<float2*>(y_mufu)[i] = make_float2(ex2_approx(v.x), ex2_approx(v.y));
-}
-
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -593,14 +570,6 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t p
 }
 
 }  // namespace
-
-cudaError_t launch_exp2_check(const float* x, float* y_fma, float* y_mufu, int64_t n, cudaStream_t s)
-{
-    const int64_t npairs = n / 2;
-    if (npairs == 0) return cudaSuccess;
-    exp2_check_kernel<<<static_cast<unsigned>((npairs + 255) / 256), 256, 0, s>>>(x, y_fma, y_mufu, npairs);
-    return cudaGetLastError();
-}
 
 int choose_kv_splits(int64_t items, int min_tiles, int slots)
 {

@@ -237,17 +237,6 @@ void sdv2_debug_set_kv_splits(int32_t splits) { g_force_splits.store(splits < 0 
 
 int32_t sdv2_last_kv_splits(void) { return g_last_splits; }
 
-sdv2_status sdv2_debug_exp2(const float* x, float* y_fma, float* y_mufu, int64_t n, void* stream)
-{
-    if (!x || !y_fma || !y_mufu || !aligned16(x) || !aligned16(y_fma) || !aligned16(y_mufu))
-        return fail(SDV2_ERR_INVALID_ARG, "x, y_fma and y_mufu must be non-null and 16-byte aligned");
-    if (n < 0 || (n & 1)) return fail(SDV2_ERR_INVALID_ARG, "n must be even and >= 0");
-    sdv2_status s = check_device();
-    if (s != SDV2_OK) return s;
-    return cuda_status(sdv2::launch_exp2_check(x, y_fma, y_mufu, n, static_cast<cudaStream_t>(stream)),
-                       "exp2 check launch");
-}
-
 size_t sdv2_workspace_bytes(const sdv2_stream_cfg* c)
 {
     if (check_cfg(c) != SDV2_OK) return 0;

@@ -91,9 +91,6 @@ cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cach
 // loops have at least `min_tiles` tiles (ties go to fewer splits).
 int choose_kv_splits(int64_t items, int min_tiles, int slots);
 
-// The softmax's two exponentials (FMA-pipe polynomial and ex2.approx) on n values (n even).
-cudaError_t launch_exp2_check(const float* x, float* y_fma, float* y_mufu, int64_t n, cudaStream_t s);
-
 // ---- motion -----------------------------------------------------------------------------------
 
 cudaError_t launch_motion_l2(const uint8_t* frames, int B, int64_t T, int64_t frame_bytes,

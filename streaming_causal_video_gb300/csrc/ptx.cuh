@@ -259,48 +259,4 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
-__device__ __forceinline__ uint64_t fadd2_rm(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// 2^x of two fp32 values on the FMA pipe instead of the MUFU unit.  Range reduction by the power
-// of two (x = n + f, n = floor(x), f in [0, 1)) and a cubic for 2^f whose coefficients minimise
-// the maximum relative error on [0, 1] (Remez exchange; streaming_causal_video_gb300/exp2_poly.py
-// computes them and models this arithmetic bit for bit).  Relative error <= 7.5e-5 for
-// x in [-125, 8]; x below -126 gives about 2^-126 (no NaN: the clamp keeps the exponent field
-// from wrapping).  -inf gives 2^-126.
-constexpr float kExp2Magic = 12582912.0f;        // 1.5 * 2^23: j's low mantissa bits hold floor(x)
-constexpr float kExp2C0 = 9.999251962e-01f;
-constexpr float kExp2C1 = 6.958335638e-01f;
-constexpr float kExp2C2 = 2.260671556e-01f;
-constexpr float kExp2C3 = 7.802452147e-02f;
-
-__device__ __forceinline__ void exp2_fma_x2(uint64_t x, float& y0, float& y1)
-{
-    float x0, x1;
-    f32x2_unpack(x, x0, x1);
-    const uint64_t xc = f32x2_pack(fmaxf(x0, -126.0f), fmaxf(x1, -126.0f));
-    const uint64_t magic = f32x2_pack(kExp2Magic, kExp2Magic);
-    const uint64_t j = fadd2_rm(xc, magic);                 // floor(x) + 1.5 * 2^23
-    const uint64_t f = fsub2(xc, fsub2(j, magic));          // x - floor(x), exact
-    uint64_t p = ffma2(f32x2_pack(kExp2C3, kExp2C3), f, f32x2_pack(kExp2C2, kExp2C2));
-    p = ffma2(p, f, f32x2_pack(kExp2C1, kExp2C1));
-    p = ffma2(p, f, f32x2_pack(kExp2C0, kExp2C0));
-    float p0, p1, j0, j1;
-    f32x2_unpack(p, p0, p1);
-    f32x2_unpack(j, j0, j1);
-    y0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(j0) << 23));   // 2^floor(x) into the exponent
-    y1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(j1) << 23));
-}
-
 }  // namespace sdv2

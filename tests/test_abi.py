@@ -27,7 +27,7 @@ def header_functions():
 
 def test_library_exports_every_declared_function():
     declared = header_functions()
-    assert len(declared) == 23, declared
+    assert len(declared) == 22, declared
     L = sd.lib()
     missing = [n for n in declared if not hasattr(L, n)]
     assert not missing, missing
