@@ -152,7 +152,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -163,10 +163,15 @@ class ClockSampler:
                 smax.append(float(parts[1]))
             except ValueError:
                 continue
+            try:
+                power.append(float(parts[2]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w": statistics.median(power) if power else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -363,12 +368,15 @@ def timed_steps(state, steps, dist, dev, clock_gpu, attn_ev=None, rope_ev=None):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(state.stream)
     flops = 0.0
+    h0 = time.perf_counter()
     for _ in range(steps):
         flops += state.step(attn_ev, rope_ev)
+    clocks.host_issue_ms_per_step = (time.perf_counter() - h0) * 1e3 / max(1, steps)
     t1.record(state.stream)
     torch.cuda.synchronize(dev)
     dist.barrier()
     clk = clocks.stop()
+    clk["host_issue_ms_per_step"] = round(clocks.host_issue_ms_per_step, 3)
     return flops, dist.max(t0.elapsed_time(t1)), clk
 
 
@@ -512,8 +520,10 @@ def run_ours(args, dist):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         f2 = 0.0
+        h0 = time.perf_counter()
         for _ in range(args.steps):
             f2 += e2e_step()
+        host_issue_ms = (time.perf_counter() - h0) * 1e3 / args.steps
         # the step's results are on the host only when both copy streams have drained
         done_h2d = torch.cuda.Event()
         done_h2d.record(h2d_stream)
@@ -529,6 +539,7 @@ def run_ours(args, dist):
         e2e = {"value": round(f2 * dist.world / (ms2 * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(ms2 / args.steps, 3),
+               "host_issue_ms_per_step": round(host_issue_ms, 3),
                "latent_frames_per_s": round(args.steps * w.chunk_frames * B * dist.world / (ms2 * 1e-3), 3),
                "copies": "pinned host buffers; H2D and D2H on two copy streams overlapped with compute"}
         del h_qkv, h_out, d_in
@@ -542,7 +553,11 @@ def run_ours(args, dist):
                 "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % peak_src,
                 "flops_per_launch": flops_per_call, "mean_launch_ms": round(attn_mean_ms, 4),
-                "launches_timed": len(attn_ms)}
+                "launches_timed": len(attn_ms),
+                "joules_per_launch_est": (round(clk["power_w"] * attn_mean_ms * 1e-3, 4)
+                                          if clk.get("power_w") else None),
+                "joules_note": "median board power sampled by nvidia-smi during the timed region x mean "
+                               "attention launch time (the step is ~97 % attention)"}
     rope_gbs = state.rope_bytes / (rope_mean_ms * 1e-3) / 1e9
     roofline_rope = {"bound": "hbm", "kernel": "rope_append_kernel", "achieved": round(rope_gbs, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(rope_gbs / hbm, 4), "traffic": None,

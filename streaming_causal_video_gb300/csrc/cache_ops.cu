@@ -29,22 +29,21 @@ __device__ __forceinline__ uint32_t rotate_pair_rr(uint32_t xy, float c, float s
     return *reinterpret_cast<const uint32_t*>(&o);
 }
 
-// Re-rotation.  Grid: z = stream * W + window slot, y = head, x covers the slot's tokens; 8 lanes
-// per token row (16 when the time segment spans more than 8 vectors), lane v handles the row's
-// v-th 16-byte vector when v < tvecs (the time segment is the first tvecs vectors of the
-// 256-byte row); each thread takes four rows, loading all four before rotating.  A slot qualifies when it holds
-// a frame of an earlier chunk (0 <= frame_id < c*F) of a stream whose current chunk is a
-// refresh chunk.  No division anywhere: the rows of one (stream, head, slot) are contiguous.
-__host__ __device__ inline int rerotate_lane_shift(int tvecs) { return tvecs <= 8 ? 3 : 4; }
+// Re-rotation.  Grid: z = stream * W + window slot, y = head, x covers the slot's rows.  Only
+// the time segment of each 256-byte key row moves: its first tvecs 16-byte vectors.  The block's
+// lanes are laid out as (row, vector < tvecs) -- 256 / tvecs rows per pass, every lane but the
+// remainder holding a live vector -- so a warp covers consecutive rows' time segments; each
+// thread takes kRerotRowsPerThread rows, all loads issued before any rotation.  A slot
+// qualifies when it holds a frame of an earlier chunk (0 <= frame_id < c*F) of a stream whose
+// current chunk is a refresh chunk.  The rows of one (stream, head, slot) are contiguous.
 constexpr int kRerotRowsPerThread = 4;
+constexpr int kRerotThreads = 256;
 
-__global__ void __launch_bounds__(256) rerotate_kernel(const __grid_constant__ RerotateParams p)
+__global__ void __launch_bounds__(kRerotThreads) rerotate_kernel(const __grid_constant__ RerotateParams p)
 {
     const int b = blockIdx.z / p.W;
     const int ws = blockIdx.z - b * p.W;                        // window slot index 0..W-1
     const int h = blockIdx.y;
-    const int lsh = rerotate_lane_shift(p.tvecs);
-    const int vec = threadIdx.x & ((1 << lsh) - 1);
     if (!p.active[b]) return;
     const int slot = p.Fs + ws;
     sdv2_slot_meta* m = p.meta + static_cast<int64_t>(b) * p.nslots + slot;
@@ -52,38 +51,45 @@ __global__ void __launch_bounds__(256) rerotate_kernel(const __grid_constant__ R
     if (fid < 0 || fid >= p.limit[b]) return;
     // the slot's time index moves even when the time segment is empty (rope_t = 0)
     if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) m->tpos -= p.shift;   // frame_id, which the others read, stays
-    if (vec >= p.tvecs) return;
-    // this thread's rows: tok0 + k * (tokens covered by the block in one pass), k < 4
-    const int per_pass = 256 >> lsh;
-    const int tok0 = blockIdx.x * per_pass * kRerotRowsPerThread + (threadIdx.x >> lsh);
+    if (p.tvecs == 0) return;
+    const int rows_per_pass = kRerotThreads / p.tvecs;
+    const int lrow = static_cast<int>(threadIdx.x) / p.tvecs;
+    const int vec = static_cast<int>(threadIdx.x) - lrow * p.tvecs;
+    if (lrow >= rows_per_pass) return;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * rows_per_pass * kRerotRowsPerThread + lrow;
     uint4* base = reinterpret_cast<uint4*>(p.k_cache + ((static_cast<int64_t>(b) * p.H + h) * p.nslots * p.HW +
-                                                        static_cast<int64_t>(slot) * p.HW) * 128);
+                                                        static_cast<int64_t>(slot) * p.HW) * 128) + vec;
+    float c[4], s[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int pr = min(vec * 4 + u, p.tp - 1);
+        c[u] = p.cs[pr].x;
+        s[u] = p.cs[pr].y;
+    }
     uint4 v[kRerotRowsPerThread];
 #pragma unroll
     for (int k = 0; k < kRerotRowsPerThread; ++k) {
-        const int tok = tok0 + k * per_pass;
-        if (tok < p.HW) v[k] = base[static_cast<int64_t>(tok) * 16 + vec];
+        const int64_t row = row0 + static_cast<int64_t>(k) * rows_per_pass;
+        if (row < p.HW) v[k] = base[row * 16];
     }
 #pragma unroll
     for (int k = 0; k < kRerotRowsPerThread; ++k) {
-        const int tok = tok0 + k * per_pass;
-        if (tok < p.HW) {
+        const int64_t row = row0 + static_cast<int64_t>(k) * rows_per_pass;
+        if (row < p.HW) {
             uint32_t* w = reinterpret_cast<uint32_t*>(&v[k]);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int pr = vec * 4 + u;
-                if (pr < p.tp) w[u] = rotate_pair_rr(w[u], p.cs[pr].x, p.cs[pr].y);
-            }
-            base[static_cast<int64_t>(tok) * 16 + vec] = v[k];
+            for (int u = 0; u < 4; ++u)
+                if (vec * 4 + u < p.tp) w[u] = rotate_pair_rr(w[u], c[u], s[u]);
+            base[row * 16] = v[k];
         }
     }
 }
 
 // Sink update.  Grid: z = stream * F_s + sink slot, y = head, x covers the slot's HW * 16
-// vectors of k and of v (contiguous for one (stream, head, slot)); each thread copies four
-// vectors of each, so that several loads are in flight.  The first thread of each slot copies
+// vectors of k and of v (contiguous for one (stream, head, slot)); each thread copies eight
+// vectors of each, all sixteen loads issued before the first store.  The first thread of each slot copies
 // the metadata.
-constexpr int kSinkVecsPerThread = 4;
+constexpr int kSinkVecsPerThread = 8;
 __global__ void __launch_bounds__(256) sink_update_kernel(const __grid_constant__ SinkUpdateParams p)
 {
     const int b = blockIdx.z / p.Fs;
@@ -161,9 +167,10 @@ __global__ void __launch_bounds__(kNoiseThreads) noise_kernel(const __grid_const
 cudaError_t launch_rerotate(const RerotateParams& p, cudaStream_t s)
 {
     if (p.B == 0 || p.W == 0 || p.HW == 0 || p.H == 0) return cudaSuccess;   // an empty time segment still moves tpos
-    const int tpb = (256 >> rerotate_lane_shift(p.tvecs)) * kRerotRowsPerThread;   // tokens per block
-    const dim3 grid(static_cast<unsigned>((p.HW + tpb - 1) / tpb), static_cast<unsigned>(p.H), static_cast<unsigned>(p.B * p.W));
-    rerotate_kernel<<<grid, 256, 0, s>>>(p);
+    const int rows_per_block = (p.tvecs > 0 ? kRerotThreads / p.tvecs : kRerotThreads) * kRerotRowsPerThread;
+    const dim3 grid(static_cast<unsigned>((p.HW + rows_per_block - 1) / rows_per_block), static_cast<unsigned>(p.H),
+                    static_cast<unsigned>(p.B * p.W));
+    rerotate_kernel<<<grid, kRerotThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

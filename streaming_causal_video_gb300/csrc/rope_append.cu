@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kVecs = 16;       // 16-byte vectors per 128-dim bf16 head row
 constexpr int kThreads = 256;   // 16 tokens per block
-constexpr int kHeadBatch = 4;   // heads whose loads are issued together
+constexpr int kHeadBatch = 3;   // heads whose loads are issued together (two batches in flight)
 
 __device__ __forceinline__ uint32_t rotate_pair(uint32_t xy, float c, float s)
 {
@@ -43,7 +43,7 @@ __device__ __forceinline__ uint4 rotate_vec(uint4 a, const float (&c)[4], const 
     return r;
 }
 
-__global__ void __launch_bounds__(kThreads) rope_append_kernel(const __grid_constant__ RopeAppendParams p)
+__global__ void __launch_bounds__(kThreads, 2) rope_append_kernel(const __grid_constant__ RopeAppendParams p)
 {
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     const int vec = static_cast<int>(gid & (kVecs - 1));
@@ -51,6 +51,25 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(const __grid_cons
     if (tok >= static_cast<int64_t>(p.B) * p.Nq) return;
     const int b = static_cast<int>(tok / p.Nq);
     const int n = static_cast<int>(tok - static_cast<int64_t>(b) * p.Nq);
+    const int64_t src = static_cast<int64_t>(b) * p.Nq * p.tok_stride + static_cast<int64_t>(n) * p.tok_stride
+                        + vec * 8;
+    const uint4* __restrict__ q = reinterpret_cast<const uint4*>(p.q + src);
+    const uint4* __restrict__ k = reinterpret_cast<const uint4*>(p.k + src);
+    const uint4* __restrict__ v = reinterpret_cast<const uint4*>(p.v + src);
+
+    // The first heads' loads go out before anything else, so that the table lookups below run
+    // while they are in flight; afterwards each batch's loads are issued before the previous
+    // batch is rotated and stored.
+    uint4 qa[kHeadBatch], ka[kHeadBatch], va[kHeadBatch];
+#pragma unroll
+    for (int u = 0; u < kHeadBatch; ++u) {
+        if (u < p.H) {
+            qa[u] = __ldg(q + u * kVecs);
+            ka[u] = __ldg(k + u * kVecs);
+            va[u] = __ldg(v + u * kVecs);
+        }
+    }
+
     const int i = n / p.HW;                            // frame of the chunk
     const int r = n - i * p.HW;                        // token inside the frame
     const int gh = r / p.grid_w;
@@ -58,36 +77,39 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(const __grid_cons
     const int fr = b * p.F + i;
     const FrameDesc fd = p.frames[fr];
 
-    // (cos, sin) of this thread's 4 pairs: pair index 4*vec + u across the t, h, w segments.
+    // (cos, sin) of this thread's 4 pairs: pair index 4*vec + u across the t, h, w segments; the
+    // table is picked by a select on its address, so that the 4 loads issue together.
     float c[4], s[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int pr = vec * 4 + u;
-        float2 cs;
-        if (pr < p.tp) cs = p.tcs[fr * p.tp + pr];
-        else if (pr < p.tp + p.hp) cs = p.h_tab[gh * p.hp + (pr - p.tp)];
-        else cs = p.w_tab[gw * p.wp + (pr - p.tp - p.hp)];
+        const float2* src_t = &p.tcs[fr * p.tp + pr];
+        const float2* src_h = p.h_tab + gh * p.hp + (pr - p.tp);
+        const float2* src_w = p.w_tab + gw * p.wp + (pr - p.tp - p.hp);
+        const float2* cs_ptr = pr < p.tp ? src_t : (pr < p.tp + p.hp ? src_h : src_w);
+        const float2 cs = *cs_ptr;
         c[u] = cs.x;
         s[u] = cs.y;
     }
 
-    const int64_t src = static_cast<int64_t>(b) * p.Nq * p.tok_stride + static_cast<int64_t>(n) * p.tok_stride
-                        + vec * 8;
     const int64_t rows = static_cast<int64_t>(p.nslots) * p.HW;
     const int64_t crow = static_cast<int64_t>(fd.slot) * p.HW + r;
-    const uint4* __restrict__ q = reinterpret_cast<const uint4*>(p.q + src);
-    const uint4* __restrict__ k = reinterpret_cast<const uint4*>(p.k + src);
-    const uint4* __restrict__ v = reinterpret_cast<const uint4*>(p.v + src);
-
     for (int h0 = 0; h0 < p.H; h0 += kHeadBatch) {
         const int nh = min(kHeadBatch, p.H - h0);
-        uint4 qa[kHeadBatch], ka[kHeadBatch], va[kHeadBatch];
+        uint4 qr[kHeadBatch], kr[kHeadBatch], vr[kHeadBatch];
 #pragma unroll
         for (int u = 0; u < kHeadBatch; ++u) {
-            if (u < nh) {
-                qa[u] = __ldg(q + (h0 + u) * kVecs);
-                ka[u] = __ldg(k + (h0 + u) * kVecs);
-                va[u] = __ldg(v + (h0 + u) * kVecs);
+            qr[u] = qa[u];
+            kr[u] = ka[u];
+            vr[u] = va[u];
+        }
+        const int h1 = h0 + kHeadBatch;                // next batch: loads issued now
+#pragma unroll
+        for (int u = 0; u < kHeadBatch; ++u) {
+            if (h1 + u < p.H) {
+                qa[u] = __ldg(q + (h1 + u) * kVecs);
+                ka[u] = __ldg(k + (h1 + u) * kVecs);
+                va[u] = __ldg(v + (h1 + u) * kVecs);
             }
         }
 #pragma unroll
@@ -97,9 +119,9 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(const __grid_cons
                 uint4* qo = reinterpret_cast<uint4*>(p.q_rot + (bh * p.Nq + n) * 128) + vec;
                 uint4* ko = reinterpret_cast<uint4*>(p.k_cache + (bh * rows + crow) * 128) + vec;
                 uint4* vo = reinterpret_cast<uint4*>(p.v_cache + (bh * rows + crow) * 128) + vec;
-                *qo = rotate_vec(qa[u], c, s);
-                *ko = rotate_vec(ka[u], c, s);
-                *vo = va[u];
+                *qo = rotate_vec(qr[u], c, s);
+                *ko = rotate_vec(kr[u], c, s);
+                *vo = vr[u];
             }
         }
     }

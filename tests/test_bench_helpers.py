@@ -76,6 +76,7 @@ def test_clock_samples_give_median_max_and_active_reasons():
              "garbage"]                                                                   # skipped
     r = _summary(lines)
     assert r["sm_mhz"] == 1905.0 and r["sm_max_mhz"] == 2070.0 and r["samples"] == 3
+    assert r["power_w"] == 1350.2
     assert r["reasons"] == ["sw_power_cap"]
     r = _summary(["1500, 2070, 900, 0x8, Active, Not Active, Active, Not Active"])
     assert r["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
