@@ -503,8 +503,15 @@ def run_ours(args, dist):
                                       sess.ws, stream)
                     in_free[i].record(stream)
                     stream.wait_event(out_free[l])
+                    if e2e_attn_ev is not None:
+                        a0 = torch.cuda.Event(enable_timing=True)
+                        a0.record(stream)
                     sd.chunk_attention(cfg, [c] * B, sess.q_rot, L.k, L.v, outs[l], sess.ws, stream=stream)
                     out_ready[l].record(stream)
+                    if e2e_attn_ev is not None:
+                        a1 = torch.cuda.Event(enable_timing=True)
+                        a1.record(stream)
+                        e2e_attn_ev.append((a0, a1))
                     with torch.cuda.stream(d2h_stream):
                         d2h_stream.wait_event(out_ready[l])
                         h_out[l].copy_(outs[l], non_blocking=True)
@@ -512,9 +519,13 @@ def run_ours(args, dist):
             state.chunk += 1
             return w.denoise_steps * w.layers * flops_per_call
 
+        e2e_attn_ev = None
         for _ in range(warmup):
             e2e_step()
         torch.cuda.synchronize(dev)
+        e2e_attn_ev = []
+        clocks2 = ClockSampler(dist.local)
+        clocks2.start()
         dist.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -534,12 +545,16 @@ def run_ours(args, dist):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         dist.barrier()
+        clk2 = clocks2.stop()
         ms2 = dist.max(e0.elapsed_time(e1))
+        e2e_attn_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_attn_ev)
         sd.check_device_error(sess.ws, stream)
         e2e = {"value": round(f2 * dist.world / (ms2 * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(ms2 / args.steps, 3),
                "host_issue_ms_per_step": round(host_issue_ms, 3),
+               "attention_mean_launch_ms": round(e2e_attn_ms, 4),
+               "clocks": clk2,
                "latent_frames_per_s": round(args.steps * w.chunk_frames * B * dist.world / (ms2 * 1e-3), 3),
                "copies": "pinned host buffers; H2D and D2H on two copy streams overlapped with compute"}
         del h_qkv, h_out, d_in

@@ -9,20 +9,21 @@
 // frame and chunk, as in sdv2_rope_append_kv) and writes q_rot (head-major) and k_rot, v into
 // the frames' cache slots, without a round trip of q, k, v through memory.
 //
-// Tiling: a CTA computes 256 tokens x 192 features as two 128-row halves, each with its own
-// fp32 accumulator in tensor memory (columns 0 and 256), over the whole hidden dimension in
-// steps of 64 (128-byte swizzled TMA boxes) through a 3-stage ring of 56 KB stages; both halves
-// multiply the same weight stage, so a stage carries 22 % fewer bytes per flop than a 128 x 256
-// tile.  One CTA per SM; 456 tiles at the Wan-1.3B 480p shape, three full waves.  A tile may
-// straddle heads and the q|k|v boundaries: the epilogue finds the type and head of each
-// 32-feature chunk.
+// Tiling: persistent CTAs, one per SM, walk the tiles of 256 tokens x 128 features (tile t,
+// t + gridDim.x, ...).  A tile is two 128-row halves, each with its own fp32 accumulator of 128
+// columns in tensor memory, so a tile holds 256 of the 512 columns and two tiles fit: the MMA
+// warp fills one accumulator buffer while the epilogue drains the other, and the epilogue of a
+// tile runs under the next tile's main loop.  The hidden dimension streams in steps of 64
+// (128-byte swizzled TMA boxes) through a 4-stage ring of 48 KB stages; both halves multiply
+// the same weight stage.  A 128-feature tile is exactly one head of q, k or v.
 //   warp 0: TMA producer; warp 1: MMA issuer (converged: every lane polls the stage barrier and
 //   a warp vote agrees on the outcome; elect.sync issues); warps 2-9: epilogue, two per TMEM lane
 //   quarter (one per half), thread = token row, with the next 32-column TMEM load in flight while
 //   the current chunk is rotated and stored (bias read as float4).  A chunk's 16 cos/sin pairs
 //   are loaded into registers before any is used: each pair's table (time, h or w axis) is
 //   picked by a pointer select, so the 16 loads issue back to back instead of one per branch
-//   of the axis test (that had left the epilogue longer than the main loop).
+//   of the axis test.  Barriers: full/empty per ring stage; accumulator full/empty per buffer
+//   (the empty one counts the eight epilogue warps).
 // Rounding: acc (fp32, fp32 accumulation) + bias (fp32 add); q and k pairs rotated in fp32 as
 // (fmaf(x, c, -(y*s)), fmaf(x, s, y*c)); one bf16 round-to-nearest-even per output.
 #include <cuda_bf16.h>
@@ -37,16 +38,23 @@ namespace sdv2 {
 namespace {
 
 constexpr int QBM = 256;                       // tokens per tile: two halves of 128 rows
-constexpr int QBN = 192;                       // features per tile
+constexpr int QBN = 128;                       // features per tile (one head of q, k or v)
 constexpr int QBK = 64;                        // hidden elements per step (128 bytes of bf16)
-constexpr int QST = 3;                         // ring stages
+constexpr int QST = 4;                         // ring stages
 constexpr uint32_t A_BYTES = QBM * QBK * 2;    // 32 KB
 constexpr uint32_t A_HALF = A_BYTES / 2;       // rows 128..255 of the A box start here
-constexpr uint32_t B_BYTES = QBN * QBK * 2;    // 24 KB
+constexpr uint32_t B_BYTES = QBN * QBK * 2;    // 16 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int QTHREADS = 10 * 32;
-constexpr uint32_t QTMEM_COLS = 512;           // accumulators at columns 0 and 256
+constexpr int QEPI_WARPS = 8;
+constexpr uint32_t QACC_COLS = 2 * QBN;        // one tile's accumulators: two halves of QBN columns
+constexpr uint32_t QTMEM_COLS = 512;           // two accumulator buffers, at columns 0 and 256
+static_assert(2 * QACC_COLS == QTMEM_COLS, "two tiles' accumulators fill tensor memory");
+// barriers: full[QST], empty[QST], acc_full[2], acc_empty[2], mma_done
+constexpr int QB_FULL = 0, QB_EMPTY = QST, QB_ACC_FULL = 2 * QST, QB_ACC_EMPTY = 2 * QST + 2,
+              QB_DONE = 2 * QST + 4, QNBARS = 2 * QST + 5;
 constexpr uint32_t QSMEM_BYTES = QST * STAGE_BYTES + 256 + 1024;
+static_assert(QNBARS * 8 + 8 <= 256, "barriers and flags fit their 256 bytes");
 static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "128-byte swizzle needs 1024-byte aligned tiles");
 static_assert(QSMEM_BYTES <= 232448, "shared memory per CTA");
 
@@ -76,30 +84,35 @@ __device__ __forceinline__ void tmem_wait_ld_tied(uint32_t (&r)[32])
                  : "memory");
 }
 
-__global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constant__ QkvRopeParams p)
+__global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_constant__ QkvRopeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s0 = smem_u32(smem);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QST * STAGE_BYTES);
     const uint32_t bar0 = smem_u32(bars);
-    // barriers: full[QST], empty[QST], acc_full
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * QST + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + QNBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 #define QBAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
     const int lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * QBM;
-    const int n0 = blockIdx.y * QBN;
+    const int ntn = 3 * p.H * 128 / QBN;                    // feature tiles
+    const int ntiles = ((p.M + QBM - 1) / QBM) * ntn;
+    const int my_tiles = static_cast<int>(blockIdx.x) < ntiles
+                             ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
     const int ksteps = p.C / QBK;
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < QST; ++i) {
-            mbar_init(QBAR(i), 1);
-            mbar_init(QBAR(QST + i), 1);
+            mbar_init(QBAR(QB_FULL + i), 1);
+            mbar_init(QBAR(QB_EMPTY + i), 1);
         }
-        mbar_init(QBAR(2 * QST), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(QBAR(QB_ACC_FULL + i), 1);
+            mbar_init(QBAR(QB_ACC_EMPTY + i), QEPI_WARPS);
+        }
+        mbar_init(QBAR(QB_DONE), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -119,24 +132,34 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
             tma_prefetch_desc(&p.wmap);
             int pend[QST] = {};
             uint32_t par[QST] = {};
-            for (int kk = 0; kk < ksteps; ++kk) {
-                const int st = kk % QST;
-                const uint32_t ph = static_cast<uint32_t>(kk / QST) & 1u;
-                if (!mbar_wait_bounded(QBAR(QST + st), ph ^ 1u, tmo, abort_flag)) {
-                    *abort_flag = 1;
-                    atomicOr(p.err, kErrTimeout);
-                    break;
+            bool ok = true;
+            int g = 0;                                       // k-steps issued so far, over all tiles
+            for (int li = 0; ok && li < my_tiles; ++li) {
+                const int tile = static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x);
+                const int m0 = (tile / ntn) * QBM;
+                const int n0 = (tile % ntn) * QBN;
+                for (int kk = 0; kk < ksteps; ++kk, ++g) {
+                    const int st = g % QST;
+                    const uint32_t ph = static_cast<uint32_t>(g / QST) & 1u;
+                    if (!mbar_wait_bounded(QBAR(QB_EMPTY + st), ph ^ 1u, tmo, abort_flag)) {
+                        *abort_flag = 1;
+                        atomicOr(p.err, kErrTimeout);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = s0 + st * STAGE_BYTES;
+                    mbar_arrive_expect_tx(QBAR(QB_FULL + st), STAGE_BYTES);
+                    tma_load_3d(sa, &p.xmap, QBAR(QB_FULL + st), kk * QBK, m0, 0);
+                    tma_load_3d(sa + A_BYTES, &p.wmap, QBAR(QB_FULL + st), kk * QBK, n0, 0);
+                    pend[st] = 1;
+                    par[st] = ph;
                 }
-                const uint32_t sa = s0 + st * STAGE_BYTES;
-                mbar_arrive_expect_tx(QBAR(st), STAGE_BYTES);
-                tma_load_3d(sa, &p.xmap, QBAR(st), kk * QBK, m0, 0);
-                tma_load_3d(sa + A_BYTES, &p.wmap, QBAR(st), kk * QBK, n0, 0);
-                pend[st] = 1;
-                par[st] = ph;
             }
+            // Drain: the last copy into each stage must land before the CTA may exit (earlier
+            // ones were consumed by the MMA warp before the stage was refilled).
             volatile int no_abort = 0;
             for (int i = 0; i < QST; ++i)
-                if (pend[i]) mbar_wait_bounded(QBAR(i), par[i], tmo, &no_abort);
+                if (pend[i]) mbar_wait_bounded(QBAR(QB_FULL + i), par[i], tmo, &no_abort);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -146,36 +169,52 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
         const uint64_t dB = sdesc_sw128(s0 + A_BYTES, 16, 1024);
         constexpr uint64_t kStage = STAGE_BYTES >> 4;
         constexpr uint64_t kHalf = A_HALF >> 4;
+        auto wait = [&](int bar_idx, uint32_t parity) -> bool {
+            const bool r = mbar_wait_bounded(QBAR(bar_idx), parity, tmo, abort_flag);
+            return __all_sync(0xffffffffu, r);
+        };
         bool ok = true;
-        for (int kk = 0; kk < ksteps; ++kk) {
-            const int st = kk % QST;
-            const bool r = mbar_wait_bounded(QBAR(st), static_cast<uint32_t>(kk / QST) & 1u, tmo, abort_flag);
-            if (!__all_sync(0xffffffffu, r)) {
+        int g = 0;
+        for (int li = 0; ok && li < my_tiles; ++li) {
+            const int buf = li & 1;
+            // the epilogue has drained this buffer's previous tile (first use: passes at once)
+            if (!wait(QB_ACC_EMPTY + buf, (static_cast<uint32_t>(li >> 1) & 1u) ^ 1u)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint64_t a = dA + static_cast<uint64_t>(st) * kStage;
-            const uint64_t b = dB + static_cast<uint64_t>(st) * kStage;
-            // both halves of the tile multiply the same weight stage
+            const uint32_t dacc = tmem + static_cast<uint32_t>(buf) * QACC_COLS;
+            for (int kk = 0; kk < ksteps; ++kk, ++g) {
+                const int st = g % QST;
+                if (!wait(QB_FULL + st, static_cast<uint32_t>(g / QST) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t a = dA + static_cast<uint64_t>(st) * kStage;
+                const uint64_t b = dB + static_cast<uint64_t>(st) * kStage;
+                // both halves of the tile multiply the same weight stage
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+                for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                for (int k = 0; k < QBK / 16; ++k)
-                    mma_ss_warp(tmem + static_cast<uint32_t>(hh * 256), a + static_cast<uint64_t>(hh) * kHalf +
-                                static_cast<uint64_t>(k * 2), b + static_cast<uint64_t>(k * 2), idesc,
-                                (kk > 0 || k > 0) ? 1u : 0u);
-            mma_commit_warp(QBAR(QST + st));
+                    for (int k = 0; k < QBK / 16; ++k)
+                        mma_ss_warp(dacc + static_cast<uint32_t>(hh * QBN),
+                                    a + static_cast<uint64_t>(hh) * kHalf + static_cast<uint64_t>(k * 2),
+                                    b + static_cast<uint64_t>(k * 2), idesc, (kk > 0 || k > 0) ? 1u : 0u);
+                mma_commit_warp(QBAR(QB_EMPTY + st));
+            }
+            if (!ok) break;
+            mma_commit_warp(QBAR(QB_ACC_FULL + buf));        // this tile's accumulators are complete
         }
         if (!ok && lane == 0) {
             *abort_flag = 1;
             atomicOr(p.err, kErrTimeout);
         }
-        mma_commit_warp(QBAR(2 * QST));   // accumulator complete (or drained after an abort)
         // Tensor memory is freed only after every MMA of this warp has completed.
+        mma_commit_warp(QBAR(QB_DONE));
         if (lane == 0) {
             volatile int no_abort = 0;
-            mbar_wait_bounded(QBAR(2 * QST), 0, tmo, &no_abort);
+            mbar_wait_bounded(QBAR(QB_DONE), 0, tmo, &no_abort);
         }
         __syncwarp();
     } else {
@@ -185,96 +224,114 @@ __global__ void __launch_bounds__(QTHREADS) qkv_rope_kernel(const __grid_constan
         const int hh = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int row = hh * 128 + quarter * 32 + lane;
-        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(hh * 256);
-        bool ok = mbar_wait_bounded(QBAR(2 * QST), 0, tmo, abort_flag) && !*abort_flag;
-        ok = __all_sync(0xffffffffu, ok);               // the TMEM loads below are warp-collective
-        if (!ok && lane == 0) atomicOr(p.err, kErrTimeout);
-        tc_fence_after();
-        const int m = m0 + row;
-        const bool valid = ok && m < p.M;
-        const int mm = valid ? m : 0;
-        const int b = mm / p.Nq;
-        const int n = mm - b * p.Nq;
-        const int i = n / p.HW;
-        const int r = n - i * p.HW;
-        const int gh = r / p.grid_w;
-        const int gw = r - gh * p.grid_w;
-        const FrameDesc fd = p.frames[b * p.F + i];
         const int hd = p.H * 128;
         const int64_t rows = static_cast<int64_t>(p.nslots) * p.HW;
-        const float2* t_row = p.tcs + (b * p.F + i) * p.tp;
-        const float2* h_row = p.h_tab + gh * p.hp;
-        const float2* w_row = p.w_tab + gw * p.wp;
-        // the next chunk's TMEM load is in flight while this chunk is rotated and stored
-        uint32_t a[2][32];
-        tmem_ld_x32_async(trow, a[0]);
-        tmem_wait_ld_tied(a[0]);
-#pragma unroll
-        for (int cchunk = 0; cchunk < QBN / 32; ++cchunk) {
-            uint32_t(&cur)[32] = a[cchunk & 1];
-            if (cchunk + 1 < QBN / 32)
-                tmem_ld_x32_async(trow + static_cast<uint32_t>((cchunk + 1) * 32), a[(cchunk + 1) & 1]);
-            if (valid) {
-                const int f0 = n0 + cchunk * 32;              // feature of cur[0]
-                const int type = f0 / hd;                     // 0 = q, 1 = k, 2 = v
-                const int fl = f0 - type * hd;
-                const int head = fl >> 7;
-                const int d0 = fl & 127;                      // first dim of the chunk in its head
-                const int64_t bh = static_cast<int64_t>(b) * p.H + head;
-                uint16_t* dst = (type == 0) ? p.q_rot + (bh * p.Nq + n) * 128 + d0
-                              : (type == 1) ? p.k_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0
-                                            : p.v_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0;
-                float bv[32];
-                if (p.bias) {
-                    const float4* b4 = reinterpret_cast<const float4*>(p.bias + f0);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const float4 t4 = b4[v];
-                        bv[4 * v] = t4.x;
-                        bv[4 * v + 1] = t4.y;
-                        bv[4 * v + 2] = t4.z;
-                        bv[4 * v + 3] = t4.w;
-                    }
+        for (int li = 0; li < my_tiles; ++li) {
+            const int buf = li & 1;
+            bool ok = mbar_wait_bounded(QBAR(QB_ACC_FULL + buf), static_cast<uint32_t>(li >> 1) & 1u, tmo, abort_flag) &&
+                      !*abort_flag;
+            ok = __all_sync(0xffffffffu, ok);               // the TMEM loads below are warp-collective
+            if (!ok) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    atomicOr(p.err, kErrTimeout);
                 }
-                float2 csv[16];
-                if (type < 2) {
+                break;
+            }
+            tc_fence_after();
+            const int tile = static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x);
+            const int m0 = (tile / ntn) * QBM;
+            const int n0 = (tile % ntn) * QBN;
+            const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                  static_cast<uint32_t>(buf) * QACC_COLS + static_cast<uint32_t>(hh * QBN);
+            const int m = m0 + row;
+            const bool valid = m < p.M;
+            const int mm = valid ? m : 0;
+            const int b = mm / p.Nq;
+            const int n = mm - b * p.Nq;
+            const int i = n / p.HW;
+            const int r = n - i * p.HW;
+            const int gh = r / p.grid_w;
+            const int gw = r - gh * p.grid_w;
+            const FrameDesc fd = p.frames[b * p.F + i];
+            const float2* t_row = p.tcs + (b * p.F + i) * p.tp;
+            const float2* h_row = p.h_tab + gh * p.hp;
+            const float2* w_row = p.w_tab + gw * p.wp;
+            // the next chunk's TMEM load is in flight while this chunk is rotated and stored
+            uint32_t a[2][32];
+            tmem_ld_x32_async(trow, a[0]);
+            tmem_wait_ld_tied(a[0]);
+#pragma unroll
+            for (int cchunk = 0; cchunk < QBN / 32; ++cchunk) {
+                uint32_t(&cur)[32] = a[cchunk & 1];
+                if (cchunk + 1 < QBN / 32)
+                    tmem_ld_x32_async(trow + static_cast<uint32_t>((cchunk + 1) * 32), a[(cchunk + 1) & 1]);
+                if (valid) {
+                    const int f0 = n0 + cchunk * 32;              // feature of cur[0]
+                    const int type = f0 / hd;                     // 0 = q, 1 = k, 2 = v
+                    const int fl = f0 - type * hd;
+                    const int head = fl >> 7;
+                    const int d0 = fl & 127;                      // first dim of the chunk in its head
+                    const int64_t bh = static_cast<int64_t>(b) * p.H + head;
+                    uint16_t* dst = (type == 0) ? p.q_rot + (bh * p.Nq + n) * 128 + d0
+                                  : (type == 1) ? p.k_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0
+                                                : p.v_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0;
+                    float bv[32];
+                    if (p.bias) {
+                        const float4* b4 = reinterpret_cast<const float4*>(p.bias + f0);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const float4 t4 = b4[v];
+                            bv[4 * v] = t4.x;
+                            bv[4 * v + 1] = t4.y;
+                            bv[4 * v + 2] = t4.z;
+                            bv[4 * v + 3] = t4.w;
+                        }
+                    }
+                    float2 csv[16];
+                    if (type < 2) {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const int pr = (d0 >> 1) + u;
+                            const float2* src = pr < p.tp ? t_row + pr
+                                              : pr < p.tp + p.hp ? h_row + (pr - p.tp) : w_row + (pr - p.tp - p.hp);
+                            csv[u] = *src;           // generic load: t pairs live in the launch parameters
+                        }
+                    }
+                    uint32_t o[16];
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
-                        const int pr = (d0 >> 1) + u;
-                        const float2* src = pr < p.tp ? t_row + pr
-                                          : pr < p.tp + p.hp ? h_row + (pr - p.tp) : w_row + (pr - p.tp - p.hp);
-                        csv[u] = *src;           // generic load: t pairs live in the launch parameters
+                        float x = __uint_as_float(cur[2 * u]);
+                        float y = __uint_as_float(cur[2 * u + 1]);
+                        if (p.bias) {
+                            x = __fadd_rn(x, bv[2 * u]);
+                            y = __fadd_rn(y, bv[2 * u + 1]);
+                        }
+                        if (type < 2) {
+                            const float2 cs = csv[u];
+                            const float xr = __fmaf_rn(x, cs.x, -__fmul_rn(y, cs.y));
+                            const float yr = __fmaf_rn(x, cs.y, __fmul_rn(y, cs.x));
+                            x = xr;
+                            y = yr;
+                        }
+                        o[u] = pack2(x, y);
                     }
-                }
-                uint32_t o[16];
+                    uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    float x = __uint_as_float(cur[2 * u]);
-                    float y = __uint_as_float(cur[2 * u + 1]);
-                    if (p.bias) {
-                        x = __fadd_rn(x, bv[2 * u]);
-                        y = __fadd_rn(y, bv[2 * u + 1]);
+                    for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+                    if (type == 1 && head == 0 && d0 == 0 && r == 0) {    // one writer per (stream, frame)
+                        sdv2_slot_meta md;
+                        md.frame_id = fd.frame;
+                        md.tpos = fd.tpos;
+                        p.meta[static_cast<int64_t>(b) * p.nslots + fd.slot] = md;
                     }
-                    if (type < 2) {
-                        const float2 cs = csv[u];
-                        const float xr = __fmaf_rn(x, cs.x, -__fmul_rn(y, cs.y));
-                        const float yr = __fmaf_rn(x, cs.y, __fmul_rn(y, cs.x));
-                        x = xr;
-                        y = yr;
-                    }
-                    o[u] = pack2(x, y);
                 }
-                uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-                for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-                if (type == 1 && head == 0 && d0 == 0 && r == 0) {    // one writer per (stream, frame)
-                    sdv2_slot_meta md;
-                    md.frame_id = fd.frame;
-                    md.tpos = fd.tpos;
-                    p.meta[static_cast<int64_t>(b) * p.nslots + fd.slot] = md;
-                }
+                if (cchunk + 1 < QBN / 32) tmem_wait_ld_tied(a[(cchunk + 1) & 1]);
             }
-            if (cchunk + 1 < QBN / 32) tmem_wait_ld_tied(a[(cchunk + 1) & 1]);
+            // every TMEM load of this buffer has completed: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(QBAR(QB_ACC_EMPTY + buf));
         }
     }
     tc_fence_before();
@@ -342,7 +399,10 @@ cudaError_t launch_qkv_rope(QkvRopeParams& p, const void* x, const void* w, int6
         }
         attr_set.fetch_or(bit);
     }
-    dim3 grid(static_cast<unsigned>((p.M + QBM - 1) / QBM), static_cast<unsigned>(3 * p.H * 128 / QBN));
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t ntiles = static_cast<int64_t>((p.M + QBM - 1) / QBM) * (3 * p.H * 128 / QBN);
+    const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(ntiles, std::max(1, sms))));
     qkv_rope_kernel<<<grid, QTHREADS, QSMEM_BYTES, s>>>(p);
     return cudaGetLastError();
 }
