@@ -186,12 +186,14 @@ sdv2_status sdv2_qkv_rope_append(const sdv2_stream_cfg* cfg, const int64_t* star
  * lse: device fp32 [B][H][Nq] natural-log log-sum-exp of the scaled scores, or NULL.
  * ws: device workspace (error word of the bounded waits; key-split scratch).
  * Numerics: bf16 tensor-core products with fp32 accumulation, online softmax in fp32.
- * Work split: one CTA per (stream, head, 256 query rows, key split); the key range of an item
- * is cut into 1-4 splits chosen to fill whole waves of the GPU's SMs; the split that finishes
- * its keys last merges the others' partial rows with its own (log-sum-exp weights, splits
- * summed in index order, so the output does not depend on which split merges) and writes the
- * output.  The result is deterministic: the same inputs give the same bits on every call.
- * Limits: B <= 16; the device must be sm_103 (tcgen05 tensor cores).
+ * Work split: items of (stream, head, 256 query rows); the first items run whole, one CTA
+ * each, in whole waves of the GPU's SMs, and the key range of every later item is cut into 1-4
+ * splits (sdv2_debug_kv_schedule gives the choice); the split that finishes its keys last
+ * merges the others' partial rows with its own (log-sum-exp weights, splits summed in index
+ * order, so the output does not depend on which split merges) and writes the output.  The
+ * result is deterministic: the same inputs give the same bits on every call.
+ * Limits: B <= 16; B * H * ceil(Nq/256) * splits < 2^31; the device must be sm_103 (tcgen05
+ * tensor cores).
  */
 sdv2_status sdv2_chunk_attention(const sdv2_stream_cfg* cfg, const int64_t* chunk_index,
                                  const void* q_rot, const void* k_cache, const void* v_cache,
@@ -332,8 +334,17 @@ void sdv2_debug_drop_kv_tile(int64_t tile);
  * 1..4 = forced (capped by the number of key tiles).  For tests and tuning. */
 void sdv2_debug_set_kv_splits(int32_t splits);
 
-/* Split count used by this thread's most recent sdv2_chunk_attention call. */
+/* Split count of the split items in this thread's most recent sdv2_chunk_attention call (1 if
+ * no item was split). */
 int32_t sdv2_last_kv_splits(void);
+
+/* The automatic work schedule of sdv2_chunk_attention, for tests (host only, no GPU): for
+ * `items` = B * H * ceil(Nq/256) (stream, head, 256 query rows) items whose key loops have at
+ * least `min_tiles` 128-key tiles, on a GPU with `sms` SMs, returns the key-range split count of
+ * the split items and sets *full_items to the number of items that run whole (the first ones,
+ * in whole waves of `sms`); -1 on invalid arguments.  The schedule minimises the estimated
+ * makespan: k whole waves of unsplit items, then the rest cut into s key ranges. */
+int32_t sdv2_debug_kv_schedule(int64_t items, int32_t min_tiles, int32_t sms, int32_t* full_items);
 
 const char* sdv2_status_string(sdv2_status s);
 const char* sdv2_last_error(void);

@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     chunk_attention,
     chunk_attention_noalloc,
     debug_drop_kv_tile,
+    debug_kv_schedule,
     debug_set_kv_splits,
     last_kv_splits,
     exported_symbols,

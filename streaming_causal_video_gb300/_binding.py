@@ -16,7 +16,7 @@ EXPORTS = ["sdv2_workspace_bytes", "sdv2_cache_bytes", "sdv2_meta_bytes", "sdv2_
            "sdv2_chunk_attention_noalloc", "sdv2_noalloc_check_device_error",
            "sdv2_motion_l2", "sdv2_rope_refresh_rerotate", "sdv2_sink_update", "sdv2_noise_from_motion",
            "sdv2_check_device_error", "sdv2_set_wait_timeout_ns",
-           "sdv2_debug_drop_kv_tile", "sdv2_debug_set_kv_splits", "sdv2_last_kv_splits",
+           "sdv2_debug_drop_kv_tile", "sdv2_debug_set_kv_splits", "sdv2_last_kv_splits", "sdv2_debug_kv_schedule",
            "sdv2_status_string", "sdv2_last_error"]
 
 
@@ -113,6 +113,8 @@ def lib():
         L.sdv2_debug_set_kv_splits.argtypes = [i32]
         L.sdv2_last_kv_splits.restype = i32
         L.sdv2_last_kv_splits.argtypes = []
+        L.sdv2_debug_kv_schedule.restype = i32
+        L.sdv2_debug_kv_schedule.argtypes = [i64, i32, i32, ctypes.POINTER(ctypes.c_int32)]
         L.sdv2_status_string.restype = ctypes.c_char_p
         L.sdv2_status_string.argtypes = [ctypes.c_int]
         L.sdv2_last_error.restype = ctypes.c_char_p
@@ -304,6 +306,15 @@ def debug_drop_kv_tile(tile: int):
 
 def debug_set_kv_splits(n: int):
     lib().sdv2_debug_set_kv_splits(int(n))
+
+
+def debug_kv_schedule(items: int, min_tiles: int, sms: int):
+    """(full_items, splits) of the attention's automatic schedule; host only."""
+    full = ctypes.c_int32(0)
+    sp = lib().sdv2_debug_kv_schedule(int(items), int(min_tiles), int(sms), ctypes.byref(full))
+    if sp < 0:
+        raise ValueError("invalid schedule arguments")
+    return full.value, sp
 
 
 def last_kv_splits() -> int:

@@ -44,6 +44,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <climits>
 #include <atomic>
 #include <cmath>
 
@@ -105,6 +106,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Work unit (blockIdx.x) -> (item, key split, splits of the item).  Items are (stream, head,
+// query pair) in that order; the first p.full_items run whole (one unit each, dispatched first),
+// every later item is cut into p.splits key ranges.
+__device__ __forceinline__ void decode_unit(const AttnParams& p, int& item, int& sp, int& nsp)
+{
+    const int unit = blockIdx.x;
+    if (unit < p.full_items) {
+        item = unit;
+        sp = 0;
+        nsp = 1;
+    } else {
+        const int u = unit - p.full_items;
+        item = p.full_items + u / p.splits;
+        sp = u - (u / p.splits) * p.splits;
+        nsp = p.splits;
+    }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __grid_constant__ AttnParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -121,14 +140,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
 
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
     const int lane = threadIdx.x & 31;
-    const int qp = blockIdx.x / p.splits;           // query pair (256 rows)
-    const int sp = blockIdx.x - qp * p.splits;      // key-range split
-    const int h = blockIdx.y;
-    const int b = blockIdx.z;
+    int item_i, sp, nsp;
+    decode_unit(p, item_i, sp, nsp);
+    // the epilogue reads the unit back from shared memory rather than keeping it in registers
+    volatile int* unit_info = reinterpret_cast<volatile int*>(tmem_slot + 4);
+    if (threadIdx.x == 0) {
+        unit_info[0] = item_i;
+        unit_info[1] = sp;
+        unit_info[2] = nsp;
+    }
+    const int qp = item_i % p.qpairs;               // query pair (256 rows)
+    const int h = (item_i / p.qpairs) % p.H;
+    const int b = item_i / (p.qpairs * p.H);
     const int nkv = p.nkv[b];
     const int tiles_all = (nkv + BN - 1) / BN;
-    const int t_begin = static_cast<int>(static_cast<int64_t>(sp) * tiles_all / p.splits);
-    const int ntiles = static_cast<int>(static_cast<int64_t>(sp + 1) * tiles_all / p.splits) - t_begin;
+    const int t_begin = static_cast<int>(static_cast<int64_t>(sp) * tiles_all / nsp);
+    const int ntiles = static_cast<int>(static_cast<int64_t>(sp + 1) * tiles_all / nsp) - t_begin;
     const int q0 = qp * (BM * NQT);
     const uint64_t tmo = p.timeout_ns;
 
@@ -369,18 +396,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
             tc_fence_before();
             mbar_arrive(BAR(B_PFULL + t));
         }
+        item_i = unit_info[0];                               // written by thread 0 before the first __syncthreads
+        sp = unit_info[1];
+        nsp = unit_info[2];
+        const int64_t item = item_i;
+        const int eb = item_i / (p.qpairs * p.H);            // stream, head, first query row again
+        const int eh = (item_i / p.qpairs) % p.H;
         const int rloc = t * BM + row;                       // row inside the CTA's 256
-        const int q = q0 + rloc;
-        const int64_t item = (static_cast<int64_t>(b) * p.H + h) * p.qpairs + qp;
+        const int q = (item_i % p.qpairs) * (BM * NQT) + rloc;
+        const int64_t pidx = item - p.full_items;            // split items: index of the partial rows
         if (ok && !mbar_wait_bounded(BAR(B_OFULL + t), 0, tmo, abort_flag)) ok = false;
         // warp-uniform from here on: the epilogue's tensor-memory loads are warp-collective
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) raise_abort(abort_flag, p.err);
         if (ok) tc_fence_after();
-        if (p.splits == 1) {
+        if (nsp == 1) {
             if (ok) {
                 const float inv = 1.0f / l_run;
-                uint16_t* dst = p.out + ((static_cast<int64_t>(b) * p.Nq + q) * p.H + h) * HD;
+                uint16_t* dst = p.out + ((static_cast<int64_t>(eb) * p.Nq + q) * p.H + eh) * HD;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
@@ -399,7 +432,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                     }
                 }
                 if (p.lse && q < p.Nq)
-                    p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + q] = (m_run + __log2f(l_run)) * kLn2;
+                    p.lse[(static_cast<int64_t>(eb) * p.H + eh) * p.Nq + q] = (m_run + __log2f(l_run)) * kLn2;
             }
         } else {
             // Split keys.  Each split takes a ticket once its main loop is done; the split with
@@ -413,14 +446,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
             int32_t* published = p.counters + static_cast<int64_t>(p.B) * p.H * p.qpairs;
             if (threadIdx.x == 0) {
                 int last = 0;
-                if (!*abort_flag) last = (atomicAdd(tickets + item, 1) == p.splits - 1) ? 1 : 0;
+                if (!*abort_flag) last = (atomicAdd(tickets + item, 1) == nsp - 1) ? 1 : 0;
                 *last_flag = last;
             }
             named_bar_sync(1, 32 * 4 * NQT);
             if (!*last_flag) {
                 if (ok) {
-                    const int64_t slot = (item * p.splits + sp) * kAttnRowsPerCta + rloc;
-                    float4* po = reinterpret_cast<float4*>(p.part_o) + (item * p.splits + sp) * (HD / 4) * kAttnRowsPerCta + rloc;
+                    const int64_t slot = (pidx * nsp + sp) * kAttnRowsPerCta + rloc;
+                    float4* po = reinterpret_cast<float4*>(p.part_o) + (pidx * nsp + sp) * (HD / 4) * kAttnRowsPerCta + rloc;
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
@@ -439,7 +472,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
             } else {
                 if (threadIdx.x == 0) {
                     const uint64_t t0 = globaltimer_ns();
-                    while (*reinterpret_cast<volatile int32_t*>(published + item) < p.splits - 1) {
+                    while (*reinterpret_cast<volatile int32_t*>(published + item) < nsp - 1) {
                         if (*abort_flag || globaltimer_ns() - t0 > tmo) {
                             raise_abort(abort_flag, p.err);
                             break;
@@ -457,9 +490,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                     float M = m_run;
 #pragma unroll
                     for (int s2 = 0; s2 < kMaxKvSplits; ++s2) {
-                        if (s2 < p.splits && s2 != sp) {
+                        if (s2 < nsp && s2 != sp) {
                             const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) +
-                                                     (item * p.splits + s2) * kAttnRowsPerCta + rloc);
+                                                     (pidx * nsp + s2) * kAttnRowsPerCta + rloc);
                             ms[s2] = ml.x;
                             ls[s2] = ml.y;
                             M = fmaxf(M, ml.x);
@@ -472,12 +505,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                     float L = 0.f;
 #pragma unroll
                     for (int s2 = 0; s2 < kMaxKvSplits; ++s2)
-                        if (s2 < p.splits) {
+                        if (s2 < nsp) {
                             ms[s2] = ex2_approx(ms[s2] - M);      // weight of split s2
                             L += ls[s2] * ms[s2];
                         }
                     const float inv = 1.0f / L;
-                    uint16_t* dst = p.out + ((static_cast<int64_t>(b) * p.Nq + q) * p.H + h) * HD;
+                    uint16_t* dst = p.out + ((static_cast<int64_t>(eb) * p.Nq + q) * p.H + eh) * HD;
                     // 32 dims at a time: this split's own rows from tensor memory, the eight float4
                     // loads of each other split together
 #pragma unroll 1
@@ -486,7 +519,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
 #pragma unroll
                         for (int v = 0; v < 8; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-                        for (int s2 = 0; s2 < p.splits; ++s2) {
+                        for (int s2 = 0; s2 < nsp; ++s2) {
                             float4 u[8];
                             if (s2 == sp) {
                                 uint32_t o[32];
@@ -497,7 +530,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                                                        __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
                             } else {
                                 const float4* src = reinterpret_cast<const float4*>(p.part_o) +
-                                                    ((item * p.splits + s2) * (HD / 4) + c * 8) * kAttnRowsPerCta + rloc;
+                                                    ((pidx * nsp + s2) * (HD / 4) + c * 8) * kAttnRowsPerCta + rloc;
 #pragma unroll
                                 for (int v = 0; v < 8; ++v) u[v] = __ldcg(src + v * kAttnRowsPerCta);
                             }
@@ -520,7 +553,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                             }
                         }
                     }
-                    if (p.lse && q < p.Nq) p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + q] = (M + __log2f(L)) * kLn2;
+                    if (p.lse && q < p.Nq) p.lse[(static_cast<int64_t>(eb) * p.H + eh) * p.Nq + q] = (M + __log2f(L)) * kLn2;
                 }
             }
         }
@@ -571,26 +604,37 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t p
 
 }  // namespace
 
-int choose_kv_splits(int64_t items, int min_tiles, int slots)
+KvSchedule choose_kv_schedule(int64_t items, int min_tiles, int slots)
 {
-    int best = 1;
+    // Estimated makespan in units of one item's key loop on one SM: k whole waves of unsplit
+    // items, then the remaining items cut into s key ranges, in ceil(units / slots) waves of 1/s
+    // each (2 % added per split phase for the partial writes and the merge).  Ties go to more
+    // unsplit items, then to fewer splits.
+    KvSchedule best{0, 1};
     double best_t = 1e300;
-    for (int sp = 1; sp <= kMaxKvSplits && sp <= min_tiles; ++sp) {
-        const double waves = std::ceil(static_cast<double>(items) * sp / slots);
-        const double t = waves / sp * (sp > 1 ? 1.02 : 1.0);   // 2 %: partial write + merge
-        if (t < best_t - 1e-9) {
-            best_t = t;
-            best = sp;
+    const int64_t S = std::max(1, slots);
+    for (int64_t k = 0; k * S <= items; ++k) {
+        const int64_t rest = items - k * S;
+        for (int sp = 1; sp <= kMaxKvSplits && sp <= std::max(1, min_tiles); ++sp) {
+            if (rest == 0 && sp > 1) break;
+            const double waves = std::ceil(static_cast<double>(rest) * sp / S);
+            const double t = static_cast<double>(k) + waves / sp * (sp > 1 ? 1.02 : 1.0);
+            if (t < best_t - 1e-9 || (std::fabs(t - best_t) <= 1e-9 && k * S > best.full_items)) {
+                best_t = t;
+                best.full_items = static_cast<int>(k * S);
+                best.splits = sp;
+            }
         }
     }
+    if (best.splits == 1) best.full_items = static_cast<int>(items);   // nothing is split
     return best;
 }
 
 cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cache, const uint16_t* v_cache, int B,
                                    int H, int Nq, int64_t rows_per_head, const int32_t* nkv, float scale,
                                    uint16_t* out, float* lse, const AttnScratch& ws, uint64_t timeout_ns,
-                                   int64_t drop_tile, int force_splits, cudaStream_t s, int* splits_used,
-                                   const char** why)
+                                   int64_t drop_tile, int force_splits, const KvSchedule* sched, cudaStream_t s,
+                                   int* splits_used, const char** why)
 {
     AttnParams p{};   // about 4.4 KB; passed by value as the launch's parameter block
     if (!encode_rows_map(&p.qmap, q_rot, Nq, static_cast<int64_t>(B) * H, static_cast<int64_t>(Nq) * HD * 2)) {
@@ -613,9 +657,19 @@ cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cach
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     p.qpairs = (Nq + kAttnRowsPerCta - 1) / kAttnRowsPerCta;
     const int64_t items = static_cast<int64_t>(B) * H * p.qpairs;
-    p.splits = force_splits > 0 ? std::min(force_splits, std::min(kMaxKvSplits, min_tiles))
-                                : choose_kv_splits(items, min_tiles, std::max(1, sms));
-    *splits_used = p.splits;
+    KvSchedule ks;
+    if (sched) ks = *sched;
+    else if (force_splits > 0) ks = KvSchedule{0, std::min(force_splits, std::min(kMaxKvSplits, min_tiles))};
+    else ks = choose_kv_schedule(items, min_tiles, std::max(1, sms));
+    if (ks.splits <= 1) ks = KvSchedule{static_cast<int>(std::min<int64_t>(items, INT32_MAX)), 1};
+    const int64_t units = ks.full_items + (items - ks.full_items) * ks.splits;
+    if (ks.full_items < 0 || ks.full_items > items || units > INT32_MAX) {
+        *why = "too many attention work units (batch * heads * ceil(Nq/256) * splits must be < 2^31)";
+        return cudaErrorInvalidConfiguration;
+    }
+    p.full_items = ks.full_items;
+    p.splits = ks.splits;
+    *splits_used = ks.splits;
     p.out = out;
     p.lse = lse;
     p.err = ws.err;
@@ -640,8 +694,7 @@ cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cach
         }
         attr_set.fetch_or(bit);
     }
-    dim3 grid(static_cast<unsigned>(p.qpairs * p.splits), static_cast<unsigned>(H), static_cast<unsigned>(B));
-    chunk_attention_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(p);
+    chunk_attention_kernel<<<static_cast<unsigned>(units), NTHREADS, SMEM_BYTES, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -237,6 +237,14 @@ void sdv2_debug_set_kv_splits(int32_t splits) { g_force_splits.store(splits < 0 
 
 int32_t sdv2_last_kv_splits(void) { return g_last_splits; }
 
+int32_t sdv2_debug_kv_schedule(int64_t items, int32_t min_tiles, int32_t sms, int32_t* full_items)
+{
+    if (items < 1 || min_tiles < 1 || sms < 1 || !full_items) return -1;
+    const sdv2::KvSchedule ks = sdv2::choose_kv_schedule(items, min_tiles, sms);
+    *full_items = ks.full_items;
+    return ks.splits;
+}
+
 size_t sdv2_workspace_bytes(const sdv2_stream_cfg* c)
 {
     if (check_cfg(c) != SDV2_OK) return 0;
@@ -373,7 +381,7 @@ sdv2_status sdv2_chunk_attention(const sdv2_stream_cfg* c, const int64_t* chunk_
         static_cast<const uint16_t*>(q_rot), static_cast<const uint16_t*>(k_cache), static_cast<const uint16_t*>(v_cache),
         c->batch, c->heads, static_cast<int>(hw_of(c) * c->chunk_frames), slots_of(c) * hw_of(c), nkv, scale,
         static_cast<uint16_t*>(out), lse, scratch, g_timeout_ns.load(), g_drop_tile.load(), g_force_splits.load(),
-        static_cast<cudaStream_t>(stream), &g_last_splits, &why);
+        nullptr, static_cast<cudaStream_t>(stream), &g_last_splits, &why);
     return cuda_status(e, why);
 }
 

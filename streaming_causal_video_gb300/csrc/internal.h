@@ -58,12 +58,13 @@ struct AttnParams {
     float* lse;                             // [B][H][Nq] or null
     uint32_t* err;                          // device error word
     int32_t* counters;                      // [2][B*H*qpairs] split tickets, published splits (0 between calls)
-    float* part_ml;                         // [items*splits][256][2] running max (log2) and sum
-    float* part_o;                          // [items*splits][256][128] unnormalised output
+    float* part_ml;                         // [split items*splits][256][2] running max (log2) and sum
+    float* part_o;                          // [split items*splits][HD/4][256][4] unnormalised output
     int32_t nkv[kMaxAttnStreams];           // valid rows per stream
     int32_t B, H, Nq;
     int32_t qpairs;                         // ceil(Nq / 256)
-    int32_t splits;                         // key-range splits per item (1..kMaxKvSplits)
+    int32_t full_items;                     // items 0..full_items-1 run whole, one unit each
+    int32_t splits;                         // key-range splits of every later item (1..kMaxKvSplits)
     float scale_log2;                       // softmax scale * log2(e)
     uint64_t timeout_ns;
     int64_t drop_tile;                      // fault injection: KV tile whose copy is skipped, or -1
@@ -78,18 +79,28 @@ struct AttnScratch {
     float* part_o;
 };
 
-// Encodes the tensor maps, picks the key-range split count (0 = automatic) and launches;
-// returns the CUDA error of the launch.  *splits_used receives the split count.
+// How the (stream, head, query pair) items are cut into CTAs: the first full_items items run
+// whole (one CTA each; a multiple of the SM count, so whole waves), every later item is cut into
+// `splits` key ranges whose partial rows are merged by the last to finish.
+struct KvSchedule {
+    int full_items;
+    int splits;
+};
+
+// The schedule with the smallest estimated makespan on `slots` SMs for `items` items whose key
+// loops have at least `min_tiles` tiles.
+KvSchedule choose_kv_schedule(int64_t items, int min_tiles, int slots);
+
+// Encodes the tensor maps, picks the schedule -- `sched` if given, else `force_splits` > 0 key
+// ranges for every item, else choose_kv_schedule -- and launches; returns the CUDA error of the
+// launch.  *splits_used receives the split count of the split items (1 if none is split).
 cudaError_t launch_chunk_attention(const uint16_t* q_rot, const uint16_t* k_cache,
                                    const uint16_t* v_cache, int B, int H, int Nq,
                                    int64_t rows_per_head, const int32_t* nkv, float scale,
                                    uint16_t* out, float* lse, const AttnScratch& ws,
                                    uint64_t timeout_ns, int64_t drop_tile, int force_splits,
-                                   cudaStream_t s, int* splits_used, const char** why);
-
-// Split count that fills whole waves of `slots` CTAs best for `items` work items whose key
-// loops have at least `min_tiles` tiles (ties go to fewer splits).
-int choose_kv_splits(int64_t items, int min_tiles, int slots);
+                                   const KvSchedule* sched, cudaStream_t s, int* splits_used,
+                                   const char** why);
 
 // ---- motion -----------------------------------------------------------------------------------
 

@@ -124,11 +124,13 @@ extern "C" sdv2_status sdv2_chunk_attention_noalloc(const sdv2_stream_cfg* cfg, 
     unsigned char* base = scratch_base(dev, st, &e);
     if (!base) return na_fail(SDV2_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
 
-    // Key splits: the automatic (or forced) choice, reduced until its partial rows fit in the array.
+    // Schedule: the automatic (or forced) choice, its split count reduced until the split items'
+    // partial rows fit in the array (with one split nothing is stored).
     const int force = debug_force_splits();
-    int splits = force > 0 ? std::min(force, std::min(kMaxKvSplits, min_tiles))
-                           : choose_kv_splits(items, min_tiles, std::max(1, sms));
-    while (splits > 1 && items * splits * kAttnRowsPerCta > kNaRows) --splits;
+    KvSchedule ks = force > 0 ? KvSchedule{0, std::min(force, std::min(kMaxKvSplits, min_tiles))}
+                              : choose_kv_schedule(items, min_tiles, std::max(1, sms));
+    while (ks.splits > 1 && (items - ks.full_items) * ks.splits * kAttnRowsPerCta > kNaRows) --ks.splits;
+    if (ks.splits <= 1) ks = KvSchedule{static_cast<int>(items), 1};
 
     // The array keeps the previous call's contents: clear the split counters (the error word
     // stays, see above).
@@ -141,8 +143,8 @@ extern "C" sdv2_status sdv2_chunk_attention_noalloc(const sdv2_stream_cfg* cfg, 
     e = launch_chunk_attention(static_cast<const uint16_t*>(q_rot), static_cast<const uint16_t*>(k_cache),
                                static_cast<const uint16_t*>(v_cache), cfg->batch, cfg->heads, nq,
                                (static_cast<int64_t>(cfg->sink_frames) + cfg->window_frames) * hw, nkv, scale,
-                               static_cast<uint16_t*>(out), lse, scratch, wait_timeout_ns(), debug_drop_tile(), splits,
-                               st, &used, &why);
+                               static_cast<uint16_t*>(out), lse, scratch, wait_timeout_ns(), debug_drop_tile(), 0,
+                               &ks, st, &used, &why);
     if (e != cudaSuccess) return na_fail(SDV2_ERR_CUDA, why);
     set_last_kv_splits(used);
     set_last_error("");

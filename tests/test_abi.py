@@ -27,7 +27,7 @@ def header_functions():
 
 def test_library_exports_every_declared_function():
     declared = header_functions()
-    assert len(declared) == 22, declared
+    assert len(declared) == 23, declared
     L = sd.lib()
     missing = [n for n in declared if not hasattr(L, n)]
     assert not missing, missing
@@ -197,3 +197,31 @@ def test_next_row_entry_points_validate_on_the_host():
     assert noise(mk(ema=1.0)) == 1 and noise(mk(ema=-0.1)) == 1
     assert noise(mk(), m=FAKE + 2) == 1 and noise(mk(), rate=None) == 1
     assert noise(mk()) not in (0, 1)          # valid arguments reach the device check (no GPU here)
+
+
+@pytest.mark.parametrize("items,tiles,sms,expect", [
+    (228, 256, 152, (152, 2)),     # 1.3B-480p: one wave of whole items, the other 76 items in halves
+    (516, 591, 152, (456, 2)),     # 1.3B-720p: three whole waves, 60 items in halves
+    (760, 256, 152, (760, 1)),     # 14B-480p: exactly five waves, nothing split
+    (912, 256, 152, (912, 1)),     # stream batch: six waves
+    (48, 53, 152, (0, 3)),         # fewer items than SMs: every item in three key ranges (one wave)
+    (2, 2, 152, (0, 2)),           # tiny: capped by the number of key tiles
+    (2, 1, 152, (2, 1)),           # one key tile: nothing to split
+    (153, 256, 152, (152, 4)),     # one item left over: cut four ways
+])
+def test_attention_schedule(items, tiles, sms, expect):
+    assert sd.debug_kv_schedule(items, tiles, sms) == expect
+
+
+def test_attention_schedule_never_worse_than_uniform_splits():
+    """The chosen schedule's estimated makespan is at most that of the best uniform split count
+    (the cost model: whole waves plus ceil(units / SMs) waves of 1/s, 2 % per split phase)."""
+    import math
+    for items in list(range(1, 700, 7)) + [1520, 3000]:
+        for tiles in (1, 2, 3, 8, 256):
+            full, s = sd.debug_kv_schedule(items, tiles, 152)
+            assert 0 <= full <= items and 1 <= s <= min(4, tiles)
+            assert (s == 1) == (full == items)
+            cost = full / 152 + math.ceil((items - full) * s / 152) / s * (1.02 if s > 1 else 1.0)
+            uni = min(math.ceil(items * u / 152) / u * (1.02 if u > 1 else 1.0) for u in range(1, min(4, tiles) + 1))
+            assert cost <= uni + 1e-9, (items, tiles, full, s, cost, uni)
