@@ -493,10 +493,17 @@ def run_ours(args, dist):
                     hq, hk, hv = h_qkv[l]
                     with torch.cuda.stream(h2d_stream):
                         h2d_stream.wait_event(in_free[i])
+                        if e2e_copy_ev is not None:
+                            c0 = torch.cuda.Event(enable_timing=True)
+                            c0.record(h2d_stream)
                         q.copy_(hq, non_blocking=True)
                         k.copy_(hk, non_blocking=True)
                         v.copy_(hv, non_blocking=True)
                         in_ready[i].record(h2d_stream)
+                        if e2e_copy_ev is not None:
+                            c1 = torch.cuda.Event(enable_timing=True)
+                            c1.record(h2d_stream)
+                            e2e_copy_ev.append((c0, c1))
                     stream.wait_event(in_ready[i])
                     L = sess.layers[l]
                     sd.rope_append_kv(cfg, w.start_frames, [c] * B, q, k, v, sess.q_rot, L.k, L.v, L.meta,
@@ -520,10 +527,12 @@ def run_ours(args, dist):
             return w.denoise_steps * w.layers * flops_per_call
 
         e2e_attn_ev = None
+        e2e_copy_ev = None
         for _ in range(warmup):
             e2e_step()
         torch.cuda.synchronize(dev)
         e2e_attn_ev = []
+        e2e_copy_ev = []
         clocks2 = ClockSampler(dist.local)
         clocks2.start()
         dist.barrier()
@@ -548,12 +557,15 @@ def run_ours(args, dist):
         clk2 = clocks2.stop()
         ms2 = dist.max(e0.elapsed_time(e1))
         e2e_attn_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_attn_ev)
+        e2e_h2d_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_copy_ev)
         sd.check_device_error(sess.ws, stream)
         e2e = {"value": round(f2 * dist.world / (ms2 * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(ms2 / args.steps, 3),
                "host_issue_ms_per_step": round(host_issue_ms, 3),
                "attention_mean_launch_ms": round(e2e_attn_ms, 4),
+               "h2d_ms_per_layer": round(e2e_h2d_ms, 4),
+               "h2d_GBs_per_layer": round(3 * qkv[0][0].numel() * 2 / (e2e_h2d_ms * 1e-3) / 1e9, 1),
                "clocks": clk2,
                "latent_frames_per_s": round(args.steps * w.chunk_frames * B * dist.world / (ms2 * 1e-3), 3),
                "copies": "pinned host buffers; H2D and D2H on two copy streams overlapped with compute"}

@@ -37,8 +37,10 @@
 namespace sdv2 {
 namespace {
 
-constexpr int QBM = 256;                       // tokens per tile: two halves of 128 rows
-constexpr int QBN = 128;                       // features per tile (one head of q, k or v)
+constexpr int QBM = 256;                       // tokens per tile: 1 or 2 halves of 128 rows
+constexpr int QBN = 128;                       // features per tile (QBM * QBN = 32768)
+constexpr int QHALVES = QBM / 128;             // 128-row accumulators per tile
+static_assert(QBM * QBN == 32768 && (QHALVES == 1 || QHALVES == 2), "a tile's accumulators span 256 columns");
 constexpr int QBK = 64;                        // hidden elements per step (128 bytes of bf16)
 constexpr int QST = 4;                         // ring stages
 constexpr uint32_t A_BYTES = QBM * QBK * 2;    // 32 KB
@@ -47,7 +49,7 @@ constexpr uint32_t B_BYTES = QBN * QBK * 2;    // 16 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int QTHREADS = 10 * 32;
 constexpr int QEPI_WARPS = 8;
-constexpr uint32_t QACC_COLS = 2 * QBN;        // one tile's accumulators: two halves of QBN columns
+constexpr uint32_t QACC_COLS = QHALVES * QBN;  // one tile's accumulators: QHALVES halves of QBN columns
 constexpr uint32_t QTMEM_COLS = 512;           // two accumulator buffers, at columns 0 and 256
 static_assert(2 * QACC_COLS == QTMEM_COLS, "two tiles' accumulators fill tensor memory");
 // barriers: full[QST], empty[QST], acc_full[2], acc_empty[2], mma_done
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                 const uint64_t b = dB + static_cast<uint64_t>(st) * kStage;
                 // both halves of the tile multiply the same weight stage
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
+                for (int hh = 0; hh < QHALVES; ++hh)
 #pragma unroll
                     for (int k = 0; k < QBK / 16; ++k)
                         mma_ss_warp(dacc + static_cast<uint32_t>(hh * QBN),
@@ -219,11 +221,15 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue: 256 threads
-        // warps 2-5 read the accumulator of rows 0..127, warps 6-9 that of rows 128..255; a warp
-        // reaches the TMEM lanes of its quarter (warp index mod 4)
-        const int hh = (warp - 2) >> 2;
+        // Two warps per TMEM lane quarter (a warp reaches the lanes of quarter warp index mod 4):
+        // with two 128-row halves, warps 2-5 read rows 0..127 and warps 6-9 rows 128..255, all
+        // columns; with one half, warps 2-5 read the first half of the columns, warps 6-9 the
+        // second.  Either way a thread drains 128 columns of one row.
+        const int part = (warp - 2) >> 2;
         const int quarter = warp & 3;
-        const int row = hh * 128 + quarter * 32 + lane;
+        const int row = (QHALVES == 2 ? part * 128 : 0) + quarter * 32 + lane;
+        const int col0 = QHALVES == 2 ? 0 : part * (QBN / 2);          // first column (feature) of this thread
+        constexpr int kEpiCols = QBN * QHALVES / 2;                    // 128
         const int hd = p.H * 128;
         const int64_t rows = static_cast<int64_t>(p.nslots) * p.HW;
         for (int li = 0; li < my_tiles; ++li) {
@@ -243,7 +249,8 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
             const int m0 = (tile / ntn) * QBM;
             const int n0 = (tile % ntn) * QBN;
             const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                  static_cast<uint32_t>(buf) * QACC_COLS + static_cast<uint32_t>(hh * QBN);
+                                  static_cast<uint32_t>(buf) * QACC_COLS +
+                                  static_cast<uint32_t>(QHALVES == 2 ? part * QBN : col0);
             const int m = m0 + row;
             const bool valid = m < p.M;
             const int mm = valid ? m : 0;
@@ -262,12 +269,12 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
             tmem_ld_x32_async(trow, a[0]);
             tmem_wait_ld_tied(a[0]);
 #pragma unroll
-            for (int cchunk = 0; cchunk < QBN / 32; ++cchunk) {
+            for (int cchunk = 0; cchunk < kEpiCols / 32; ++cchunk) {
                 uint32_t(&cur)[32] = a[cchunk & 1];
-                if (cchunk + 1 < QBN / 32)
+                if (cchunk + 1 < kEpiCols / 32)
                     tmem_ld_x32_async(trow + static_cast<uint32_t>((cchunk + 1) * 32), a[(cchunk + 1) & 1]);
                 if (valid) {
-                    const int f0 = n0 + cchunk * 32;              // feature of cur[0]
+                    const int f0 = n0 + col0 + cchunk * 32;       // feature of cur[0]
                     const int type = f0 / hd;                     // 0 = q, 1 = k, 2 = v
                     const int fl = f0 - type * hd;
                     const int head = fl >> 7;
@@ -326,7 +333,7 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                         p.meta[static_cast<int64_t>(b) * p.nslots + fd.slot] = md;
                     }
                 }
-                if (cchunk + 1 < QBN / 32) tmem_wait_ld_tied(a[(cchunk + 1) & 1]);
+                if (cchunk + 1 < kEpiCols / 32) tmem_wait_ld_tied(a[(cchunk + 1) & 1]);
             }
             // every TMEM load of this buffer has completed: hand it back to the MMA warp
             tc_fence_before();

@@ -40,7 +40,7 @@ def main():
     ap.add_argument("--peak-gbs", type=float, default=0.0, help="HBM peak (GB/s); default: MEASURED_PEAKS.json or 6800")
     ap.add_argument("--layers", type=int, default=8, help="distinct layer caches cycled (more than L2 in total)")
     ap.add_argument("--only", default="", help="comma-separated subset of: append, attention, rerotate, sink, "
-                    "qkv, cublas, unfused, motion, noise (default: all)")
+                    "qkv, cublas, unfused, motion, noise, copies (default: all)")
     args = ap.parse_args()
     only = {x.strip() for x in args.only.split(",") if x.strip()}
 
@@ -163,6 +163,23 @@ def main():
                ms=_time(unfused, 60, stream))
     del sess, qkv
     torch.cuda.empty_cache()
+
+    # size-matched reference: a plain device-to-device copy (torch copy_) moving the same bytes
+    # (half read, half written) as each HBM-bound call, over 8 buffer pairs cycled so that the
+    # set is larger than L2 -- the bandwidth a copy of that size reaches on this GPU
+    if want("copies"):
+        for label, nbytes in (("rope_append_kv", w.nq * w.heads * 1536), ("rope_refresh_rerotate", rr_bytes),
+                              ("sink_update", sink_bytes)):
+            half = nbytes // 2
+            srcs = [torch.empty(half, dtype=torch.uint8, device=dev) for _ in range(nl)]
+            dsts = [torch.empty(half, dtype=torch.uint8, device=dev) for _ in range(nl)]
+
+            def cp(i):
+                dsts[i % nl].copy_(srcs[i % nl])
+            report("reference copy_ of the bytes of sdv2_" + label, w.name, bytes_per_call=2 * half,
+                   ms=_time(cp, 60, stream))
+            del srcs, dsts
+        torch.cuda.empty_cache()
     if not (want("motion") or want("noise")):
         return out
 
