@@ -60,48 +60,6 @@ static_assert(QNBARS * 8 + 8 <= 256, "barriers and flags fit their 256 bytes");
 static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "128-byte swizzle needs 1024-byte aligned tiles");
 static_assert(QSMEM_BYTES <= 232448, "shared memory per CTA");
 
-// ---- cluster pieces (the 2-CTA form shares the token tile: each CTA loads one half and the
-// copy lands in both CTAs' shared memory) --------------------------------------------------
-
-// 3D tiled load of one box, written at the same shared-memory offset of every CTA of the
-// cluster in `cta_mask`; each destination CTA's barrier at offset `bar` receives the bytes
-// written into that CTA.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                                      int32_t c0, int32_t c1, int32_t c2, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of every CTA of the cluster arrives, then waits for all of them (release /
-// acquire: shared-memory writes and barrier initialisations before it are visible after it).
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Warp-converged commit that arrives on the barrier at offset `bar` of every CTA in `cta_mask`
-// once this thread's earlier tcgen05 operations have completed.
-__device__ __forceinline__ void mma_commit_multicast_warp(uint32_t bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
-        ::"r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -128,12 +86,6 @@ __device__ __forceinline__ void tmem_wait_ld_tied(uint32_t (&r)[32])
                  : "memory");
 }
 
-// kMC: the CTAs come in clusters of 2 that take feature tiles 2j and 2j+1 of the same token
-// rows.  Each loads one 128-row half of the token tile with a multicast copy that lands in
-// both CTAs (so the pair reads the token tile from L2 once instead of twice) and its own weight
-// tile; a ring stage may be refilled only when both CTAs' MMAs are done with it, so every
-// MMA commit arrives on the stage's empty barrier in both CTAs (count 2).
-template <bool kMC>
 __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_constant__ QkvRopeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -146,27 +98,17 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
 #define QBAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
     const int lane = threadIdx.x & 31;
-    static_assert(!kMC || QHALVES == 2, "the cluster form shares two 128-row halves");
     const int ntn = 3 * p.H * 128 / QBN;                    // feature tiles
-    const int rank = kMC ? static_cast<int>(cluster_ctarank()) : 0;
-    const int group = kMC ? static_cast<int>(blockIdx.x) >> 1 : static_cast<int>(blockIdx.x);
-    const int ngroups = kMC ? static_cast<int>(gridDim.x) >> 1 : static_cast<int>(gridDim.x);
-    const int tpg = kMC ? ntn / 2 : ntn;                    // tile groups per row of token tiles
-    const int ngt = ((p.M + QBM - 1) / QBM) * tpg;          // tile groups (a pair of tiles, or one)
-    const int my_tiles = group < ngt ? (ngt - 1 - group) / ngroups + 1 : 0;
-    // tile li of this CTA: token rows from m0, features from n0
-    auto tile_origin = [&](int li, int& m0, int& n0) {
-        const int gt = group + li * ngroups;
-        m0 = (gt / tpg) * QBM;
-        n0 = ((gt % tpg) * (kMC ? 2 : 1) + rank) * QBN;
-    };
+    const int ntiles = ((p.M + QBM - 1) / QBM) * ntn;
+    const int my_tiles = static_cast<int>(blockIdx.x) < ntiles
+                             ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
     const int ksteps = p.C / QBK;
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < QST; ++i) {
             mbar_init(QBAR(QB_FULL + i), 1);
-            mbar_init(QBAR(QB_EMPTY + i), kMC ? 2 : 1);
+            mbar_init(QBAR(QB_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(QBAR(QB_ACC_FULL + i), 1);
@@ -183,7 +125,6 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (kMC) cluster_sync_all();                            // the peer's barriers exist before any multicast
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
@@ -196,8 +137,9 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
             bool ok = true;
             int g = 0;                                       // k-steps issued so far, over all tiles
             for (int li = 0; ok && li < my_tiles; ++li) {
-                int m0, n0;
-                tile_origin(li, m0, n0);
+                const int tile = static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x);
+                const int m0 = (tile / ntn) * QBM;
+                const int n0 = (tile % ntn) * QBN;
                 for (int kk = 0; kk < ksteps; ++kk, ++g) {
                     const int st = g % QST;
                     const uint32_t ph = static_cast<uint32_t>(g / QST) & 1u;
@@ -208,13 +150,8 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                         break;
                     }
                     const uint32_t sa = s0 + st * STAGE_BYTES;
-                    // the stage's bytes: the whole token tile (with kMC half of it from the peer) + weights
                     mbar_arrive_expect_tx(QBAR(QB_FULL + st), STAGE_BYTES);
-                    if (kMC)
-                        tma_load_3d_multicast(sa + static_cast<uint32_t>(rank) * A_HALF, &p.xmap, QBAR(QB_FULL + st),
-                                              kk * QBK, m0 + rank * 128, 0, static_cast<uint16_t>(0x3));
-                    else
-                        tma_load_3d(sa, &p.xmap, QBAR(QB_FULL + st), kk * QBK, m0, 0);
+                    tma_load_3d(sa, &p.xmap, QBAR(QB_FULL + st), kk * QBK, m0, 0);
                     tma_load_3d(sa + A_BYTES, &p.wmap, QBAR(QB_FULL + st), kk * QBK, n0, 0);
                     pend[st] = 1;
                     par[st] = ph;
@@ -266,10 +203,7 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                         mma_ss_warp(dacc + static_cast<uint32_t>(hh * QBN),
                                     a + static_cast<uint64_t>(hh) * kHalf + static_cast<uint64_t>(k * 2),
                                     b + static_cast<uint64_t>(k * 2), idesc, (kk > 0 || k > 0) ? 1u : 0u);
-                if (kMC)
-                    mma_commit_multicast_warp(QBAR(QB_EMPTY + st), static_cast<uint16_t>(0x3));
-                else
-                    mma_commit_warp(QBAR(QB_EMPTY + st));
+                mma_commit_warp(QBAR(QB_EMPTY + st));
             }
             if (!ok) break;
             mma_commit_warp(QBAR(QB_ACC_FULL + buf));        // this tile's accumulators are complete
@@ -311,8 +245,9 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                 break;
             }
             tc_fence_after();
-            int m0, n0;
-            tile_origin(li, m0, n0);
+            const int tile = static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x);
+            const int m0 = (tile / ntn) * QBM;
+            const int n0 = (tile % ntn) * QBN;
             const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                   static_cast<uint32_t>(buf) * QACC_COLS +
                                   static_cast<uint32_t>(QHALVES == 2 ? part * QBN : col0);
@@ -412,9 +347,6 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
         tc_fence_after();
         tmem_dealloc(tmem, QTMEM_COLS);
     }
-    // the peer may still commit to this CTA's barriers or copy into its shared memory until it
-    // is done as well: neither CTA exits before both are
-    if (kMC) cluster_sync_all();
 #undef QBAR
 }
 
@@ -457,65 +389,28 @@ bool encode_matrix(CUtensorMap* map, const void* base, int64_t rows, int64_t col
 cudaError_t launch_qkv_rope(QkvRopeParams& p, const void* x, const void* w, int64_t x_ld, cudaStream_t s,
                             const char** why)
 {
-    const int ntn = 3 * p.H * 128 / QBN;
-    const int ntm = (p.M + QBM - 1) / QBM;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (!encode_matrix(&p.xmap, x, p.M, p.C, x_ld, QBM) || !encode_matrix(&p.wmap, w, 3LL * p.H * 128, p.C, p.C, QBN)) {
+        *why = "cuTensorMapEncodeTiled failed for x or w_qkv";
+        return cudaErrorInvalidValue;
+    }
     static std::atomic<uint64_t> attr_set{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
     const uint64_t bit = uint64_t(1) << (dev & 63);
     if (!(attr_set.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(qkv_rope_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(qkv_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(QSMEM_BYTES));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(qkv_rope_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(QSMEM_BYTES));
         if (e != cudaSuccess) {
             *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
             return e;
         }
         attr_set.fetch_or(bit);
     }
-    if (!encode_matrix(&p.wmap, w, 3LL * p.H * 128, p.C, p.C, QBN)) {
-        *why = "cuTensorMapEncodeTiled failed for w_qkv";
-        return cudaErrorInvalidValue;
-    }
-
-    // Pairs of feature tiles share their token tile through a 2-CTA cluster when the feature
-    // tiles pair up and the GPU can hold such clusters.
-    if (ntn % 2 == 0) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(QTHREADS, 1, 1);
-        cfg.dynamicSmemBytes = QSMEM_BYTES;
-        cfg.stream = s;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        const int64_t groups = static_cast<int64_t>(ntm) * (ntn / 2);
-        cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min<int64_t>(groups, std::max(1, sms / 2))), 1, 1);
-        int max_clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&max_clusters, qkv_rope_kernel<true>, &cfg) == cudaSuccess &&
-            max_clusters > 0) {
-            if (!encode_matrix(&p.xmap, x, p.M, p.C, x_ld, 128)) {
-                *why = "cuTensorMapEncodeTiled failed for x";
-                return cudaErrorInvalidValue;
-            }
-            cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min<int64_t>(groups, max_clusters)), 1, 1);
-            return cudaLaunchKernelEx(&cfg, qkv_rope_kernel<true>, p);
-        }
-        cudaGetLastError();   // an occupancy query that failed leaves no sticky error; clear it
-    }
-    if (!encode_matrix(&p.xmap, x, p.M, p.C, x_ld, QBM)) {
-        *why = "cuTensorMapEncodeTiled failed for x";
-        return cudaErrorInvalidValue;
-    }
-    const int64_t ntiles = static_cast<int64_t>(ntm) * ntn;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t ntiles = static_cast<int64_t>((p.M + QBM - 1) / QBM) * (3 * p.H * 128 / QBN);
     const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(ntiles, std::max(1, sms))));
-    qkv_rope_kernel<false><<<grid, QTHREADS, QSMEM_BYTES, s>>>(p);
+    qkv_rope_kernel<<<grid, QTHREADS, QSMEM_BYTES, s>>>(p);
     return cudaGetLastError();
 }
 
