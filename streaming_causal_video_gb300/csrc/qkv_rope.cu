@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
 #define QBAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
     const int lane = threadIdx.x & 31;
-    const int ntn = 3 * p.H * 128 / QBN;                    // feature tiles
+    const int ntn = (3 * p.H * 128 + QBN - 1) / QBN;        // feature tiles (the last may be ragged)
     const int ntiles = ((p.M + QBM - 1) / QBM) * ntn;
     const int my_tiles = static_cast<int>(blockIdx.x) < ntiles
                              ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
@@ -273,8 +273,8 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                 uint32_t(&cur)[32] = a[cchunk & 1];
                 if (cchunk + 1 < kEpiCols / 32)
                     tmem_ld_x32_async(trow + static_cast<uint32_t>((cchunk + 1) * 32), a[(cchunk + 1) & 1]);
-                if (valid) {
-                    const int f0 = n0 + col0 + cchunk * 32;       // feature of cur[0]
+                const int f0 = n0 + col0 + cchunk * 32;           // feature of cur[0]
+                if (valid && f0 < 3 * hd) {                       // features past 3*H*D: zero-filled weight rows
                     const int type = f0 / hd;                     // 0 = q, 1 = k, 2 = v
                     const int fl = f0 - type * hd;
                     const int head = fl >> 7;
@@ -408,7 +408,7 @@ cudaError_t launch_qkv_rope(QkvRopeParams& p, const void* x, const void* w, int6
     }
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t ntiles = static_cast<int64_t>((p.M + QBM - 1) / QBM) * (3 * p.H * 128 / QBN);
+    const int64_t ntiles = static_cast<int64_t>((p.M + QBM - 1) / QBM) * ((3 * p.H * 128 + QBN - 1) / QBN);
     const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(ntiles, std::max(1, sms))));
     qkv_rope_kernel<<<grid, QTHREADS, QSMEM_BYTES, s>>>(p);
     return cudaGetLastError();

@@ -5,8 +5,6 @@ import json
 import os
 import threading
 
-import pytest
-
 import bench
 
 CSRC = os.path.join(bench.ROOT, "streaming_causal_video_gb300", "csrc")
@@ -84,47 +82,6 @@ def test_clock_samples_give_median_max_and_active_reasons():
 
 
 # The text of get_encode_tiled in the build the ncu traffic record was captured on.
-_CAPTURED_GET_ENCODE_TILED = '''EncodeTiledFn get_encode_tiled()
-{
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}'''
-
-
-def test_traffic_record_differs_from_its_capture_only_in_the_encoder_lookup():
-    """The record's changes_since_capture claim, checked: with the captured text of
-    get_encode_tiled put back, the current sources hash to the captured hash."""
-    path = os.path.join(bench.ROOT, "profiles", "chunk_attention_wan13b_480p.json")
-    with open(path) as fh:
-        rec = json.load(fh)
-    if "captured_source_hash" not in rec:
-        pytest.skip("the traffic record carries no captured_source_hash: it was captured on the sources it names")
-    if rec["source_hash"] != bench.attention_source_hash():
-        assert bench.profiled_traffic("wan13b_480p") is None
-        pytest.skip("the traffic record predates the current attention source: the bench reports traffic null")
-    start_tag = "EncodeTiledFn get_encode_tiled()"
-
-    def captured(f):
-        text = _read(f)
-        if f != "attention.cu":
-            return text
-        a = text.index(start_tag)
-        b = text.index("    return fn;\n}", a) + len("    return fn;\n}")
-        return text[:a] + _CAPTURED_GET_ENCODE_TILED + text[b:]
-    assert bench.attention_source_hash(captured) == rec["captured_source_hash"]
-    assert bench.attention_source_hash() == rec["source_hash"]
-
-
 def test_cpu_baseline_entry_times_attention_rope_append_and_motion():
     """The bench's CPU-baseline leg on the tiny workload with short samples: all three parts of
     the path are timed on all cores and on one thread, with their units and core counts."""
