@@ -265,6 +265,27 @@ def oracle_rope_append_sample(w, seconds_target):
     return done, t_total, 1536.0 * w.nq * w.heads
 
 
+def oracle_tiny_run():
+    """The oracle's whole tiny-stream run: every chunk appended (Causal-RoPE + list cache) and
+    every query row of every head attended.  Returns (attention flops, seconds)."""
+    import numpy as np
+    import oracle
+    from synth_inputs import qkv_chunk_bits
+    w = WORKLOADS["tiny"]
+    so = oracle.StreamOracle(w, w.start_frames[0])
+    flops, secs = 0.0, 0.0
+    for c in range(w.chunks):
+        q, k, v = qkv_chunk_bits(w, 1, c)
+        t0 = time.perf_counter()
+        q_rot = so.append_chunk(c, q[0], k[0], v[0])
+        nkv = sum(e[2].shape[0] for e in so.cache.entries)
+        for h in range(w.heads):
+            so.attend(q_rot, h)
+        secs += time.perf_counter() - t0
+        flops += 4.0 * w.heads * w.head_dim * w.nq * nkv
+    return flops, secs
+
+
 def oracle_motion_sample(frames_np, seconds_target):
     """Time the oracle's exact SSD over the given frames [B][T+1][...] repeatedly.  Returns
     (passes, seconds, bytes per pass)."""
@@ -657,6 +678,17 @@ def cpu_baseline_entry(w, motion_np, seconds=10.0, single_seconds=3.0, rope_seco
                               "rope_spec of the chunk's q and k (%d tokens x %d heads) + FrameListCache.append "
                               "of its %d frames; GB/s counts the kernel's 1536 algorithmic bytes per token-head"
                               % (w.nq, w.heads, w.chunk_frames))
+    f_all, s_all = oracle_tiny_run()
+    oracle.set_num_threads(1)
+    try:
+        f_one, s_one = oracle_tiny_run()
+    finally:
+        oracle.set_num_threads(all_threads)
+    out["tiny_run"] = {"value": round(s_all, 4), "unit": "s per run", "cores": all_threads,
+                       "single_thread_value": round(s_one, 4), "kind": "oracle",
+                       "tflops": round(f_all / s_all / 1e12, 6), "single_thread_tflops": round(f_one / s_one / 1e12, 7),
+                       "sample": "the whole tiny stream (10 chunks, 2 heads, 72 queries per chunk): Causal-RoPE + "
+                                 "list-cache append of every chunk and attention of every query row"}
     if motion_np is not None:
         out["motion"] = both(lambda: oracle_motion_sample(motion_np, motion_seconds), 1e9, "GB/s",
                              "motion_ssd of the step's %d frames of %s per stream (exact uint64), GB/s of "

@@ -9,17 +9,21 @@
 // frame and chunk, as in sdv2_rope_append_kv) and writes q_rot (head-major) and k_rot, v into
 // the frames' cache slots, without a round trip of q, k, v through memory.
 //
-// Tiling: persistent CTAs, one per SM, walk the tiles of 256 tokens x 128 features (tile t,
-// t + gridDim.x, ...).  A tile is two 128-row halves, each with its own fp32 accumulator of 128
-// columns in tensor memory, so a tile holds 256 of the 512 columns and two tiles fit: the MMA
-// warp fills one accumulator buffer while the epilogue drains the other, and the epilogue of a
-// tile runs under the next tile's main loop.  The hidden dimension streams in steps of 64
-// (128-byte swizzled TMA boxes) through a 4-stage ring of 48 KB stages; both halves multiply
-// the same weight stage.  A 128-feature tile is exactly one head of q, k or v.
+// Tiling: persistent CTAs, one per SM, walk the tiles of 128 tokens x 256 features (tile t,
+// t + gridDim.x, ...; the constants also allow two 128-row halves per tile).  A tile's fp32
+// accumulator takes 256 of the 512 tensor-memory columns, so two tiles fit: the MMA warp fills
+// one accumulator buffer while the epilogue drains the other, and the epilogue of a tile runs
+// under the next tile's main loop.  The hidden dimension streams in steps of 64 (128-byte
+// swizzled TMA boxes) through a 4-stage ring of 48 KB stages.  N = 256 MMAs read their
+// operands from shared memory at 96 bytes per cycle (a 256 x 128 tile as two M = 128 halves
+// needs 128, the whole shared-memory bandwidth) and take half as many instructions.  A tile
+// spans two heads of q, k or v; the last feature tile may be ragged (its weight rows past the
+// end load as zeros and the epilogue skips them).
 //   warp 0: TMA producer; warp 1: MMA issuer (converged: every lane polls the stage barrier and
 //   a warp vote agrees on the outcome; elect.sync issues); warps 2-9: epilogue, two per TMEM lane
 //   quarter (one per half), thread = token row, with the next 32-column TMEM load in flight while
-//   the current chunk is rotated and stored (bias read as float4).  A chunk's 16 cos/sin pairs
+//   the current chunk is rotated and stored (bias read as float4); with one 128-row half the two
+//   warps of a quarter take the two halves of the columns.  A chunk's 16 cos/sin pairs
 //   are loaded into registers before any is used: each pair's table (time, h or w axis) is
 //   picked by a pointer select, so the 16 loads issue back to back instead of one per branch
 //   of the axis test.  Barriers: full/empty per ring stage; accumulator full/empty per buffer
@@ -37,10 +41,11 @@
 namespace sdv2 {
 namespace {
 
-constexpr int QBM = 256;                       // tokens per tile: 1 or 2 halves of 128 rows
-constexpr int QBN = 128;                       // features per tile (QBM * QBN = 32768)
+constexpr int QBM = 128;                       // tokens per tile: 1 or 2 halves of 128 rows
+constexpr int QBN = 256;                       // features per tile
 constexpr int QHALVES = QBM / 128;             // 128-row accumulators per tile
-static_assert(QBM * QBN == 32768 && (QHALVES == 1 || QHALVES == 2), "a tile's accumulators span 256 columns");
+static_assert((QHALVES == 1 || QHALVES == 2) && QHALVES * QBN <= 256 && QBN % 64 == 0 && QBN <= 256,
+              "a tile's accumulators fit in one 256-column buffer; the epilogue splits them in 32-column chunks");
 constexpr int QBK = 64;                        // hidden elements per step (128 bytes of bf16)
 constexpr int QST = 4;                         // ring stages
 constexpr uint32_t A_BYTES = QBM * QBK * 2;    // 32 KB
@@ -49,9 +54,8 @@ constexpr uint32_t B_BYTES = QBN * QBK * 2;    // 16 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int QTHREADS = 10 * 32;
 constexpr int QEPI_WARPS = 8;
-constexpr uint32_t QACC_COLS = QHALVES * QBN;  // one tile's accumulators: QHALVES halves of QBN columns
+constexpr uint32_t QACC_COLS = 256;            // accumulator buffer stride: QHALVES halves of QBN columns each
 constexpr uint32_t QTMEM_COLS = 512;           // two accumulator buffers, at columns 0 and 256
-static_assert(2 * QACC_COLS == QTMEM_COLS, "two tiles' accumulators fill tensor memory");
 // barriers: full[QST], empty[QST], acc_full[2], acc_empty[2], mma_done
 constexpr int QB_FULL = 0, QB_EMPTY = QST, QB_ACC_FULL = 2 * QST, QB_ACC_EMPTY = 2 * QST + 2,
               QB_DONE = 2 * QST + 4, QNBARS = 2 * QST + 5;
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
         const int quarter = warp & 3;
         const int row = (QHALVES == 2 ? part * 128 : 0) + quarter * 32 + lane;
         const int col0 = QHALVES == 2 ? 0 : part * (QBN / 2);          // first column (feature) of this thread
-        constexpr int kEpiCols = QBN * QHALVES / 2;                    // 128
+        constexpr int kEpiCols = QBN * QHALVES / 2;                    // columns one thread drains
         const int hd = p.H * 128;
         const int64_t rows = static_cast<int64_t>(p.nslots) * p.HW;
         for (int li = 0; li < my_tiles; ++li) {

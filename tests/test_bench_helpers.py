@@ -95,5 +95,7 @@ def test_cpu_baseline_entry_times_attention_rope_append_and_motion():
         d = out[part]
         assert d["unit"] == "GB/s" and d["value"] > 0 and d["single_thread_value"] > 0
         assert d["cores"] >= 1 and d["kind"] == "oracle"
+    t = out["tiny_run"]
+    assert t["unit"] == "s per run" and t["value"] > 0 and t["single_thread_value"] > 0 and t["tflops"] > 0
     assert "motion" not in bench.cpu_baseline_entry(w, None, seconds=0.1, single_seconds=0.05,
                                                     rope_seconds=0.05)
