@@ -9,16 +9,17 @@
 // frame and chunk, as in sdv2_rope_append_kv) and writes q_rot (head-major) and k_rot, v into
 // the frames' cache slots, without a round trip of q, k, v through memory.
 //
-// Tiling: persistent CTAs, one per SM, walk the tiles of 128 tokens x 256 features (tile t,
+// Tiling: persistent CTAs, one per SM, walk the tiles of 128 tokens x 192 features (tile t,
 // t + gridDim.x, ...; the constants also allow two 128-row halves per tile).  A tile's fp32
 // accumulator takes 256 of the 512 tensor-memory columns, so two tiles fit: the MMA warp fills
 // one accumulator buffer while the epilogue drains the other, and the epilogue of a tile runs
 // under the next tile's main loop.  The hidden dimension streams in steps of 64 (128-byte
-// swizzled TMA boxes) through a 4-stage ring of 48 KB stages.  N = 256 MMAs read their
-// operands from shared memory at 96 bytes per cycle (a 256 x 128 tile as two M = 128 halves
-// needs 128, the whole shared-memory bandwidth) and take half as many instructions.  A tile
-// spans two heads of q, k or v; the last feature tile may be ragged (its weight rows past the
-// end load as zeros and the epilogue skips them).
+// swizzled TMA boxes) through a 4-stage ring of 40 KB stages.  N = 192 MMAs read their
+// operands from shared memory at 107 bytes per cycle (a 256 x 128 tile as two M = 128 halves
+// needs 128, the whole shared-memory bandwidth), and 4680 x 4608 makes 888 tiles, 5.84 per SM
+// (128 x 256: 666 tiles, 4.38 per SM, 5 on some).  A tile may straddle heads and the q|k|v
+// boundaries (the epilogue finds the type and head of each 32-feature chunk); the last feature
+// tile may be ragged (its weight rows past the end load as zeros and the epilogue skips them).
 //   warp 0: TMA producer; warp 1: MMA issuer (converged: every lane polls the stage barrier and
 //   a warp vote agrees on the outcome; elect.sync issues); warps 2-9: epilogue, two per TMEM lane
 //   quarter (one per half), thread = token row, with the next 32-column TMEM load in flight while
@@ -42,7 +43,7 @@ namespace sdv2 {
 namespace {
 
 constexpr int QBM = 128;                       // tokens per tile: 1 or 2 halves of 128 rows
-constexpr int QBN = 256;                       // features per tile
+constexpr int QBN = 192;                       // features per tile
 constexpr int QHALVES = QBM / 128;             // 128-row accumulators per tile
 static_assert((QHALVES == 1 || QHALVES == 2) && QHALVES * QBN <= 256 && QBN % 64 == 0 && QBN <= 256,
               "a tile's accumulators fit in one 256-column buffer; the epilogue splits them in 32-column chunks");
