@@ -10,10 +10,11 @@
 //
 // How (one CTA = one head of one stream, two 128-row query tiles and one key split):
 //   warps 8, 10 (TMA): Q tiles once, then K (warp 8, 3-stage ring) and V (warp 10, 2-stage ring)
-//                       tiles of 128 keys; every fourth query pair of a head also prefetches them
-//                       into L2 four tiles ahead.  3D tensor maps per stream clip the key range at
-//                       the valid prefix, so rows past it arrive as zeros; 128-byte swizzled boxes
-//                       of 64 dims.
+//                       tiles of 128 keys.  The CTAs of one head walk the same keys at about the
+//                       same time, so most tiles come from L2 (explicit L2 prefetches measured
+//                       slower).  3D tensor maps per stream clip the key range at the valid
+//                       prefix, so rows past it arrive as zeros; 128-byte swizzled boxes of 64
+//                       dims.
 //   warp 9 (MMA)      : runs converged: every lane polls each barrier and a warp vote agrees on
 //                       the outcome; an elected lane issues each tcgen05.mma.  S_t = Q_t K^T
 //                       (A and B from shared memory, K-major) into tensor memory;
@@ -66,7 +67,6 @@ constexpr int TMA_WARP = 4 * NQT;        // Q and K tiles
 constexpr int MMA_WARP = 4 * NQT + 1;    // MMA issue (also allocates tensor memory)
 constexpr int TMA_V_WARP = 4 * NQT + 2;  // V tiles
 constexpr int NTHREADS = (4 * NQT + 3) * 32;
-constexpr int PREFETCH_TILES = 4;        // K/V tiles prefetched into L2 ahead of their load
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
@@ -184,10 +184,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
     if (warp == TMA_WARP || warp == TMA_V_WARP) {
         // ------------------------------------------------------------------ producers (TMA)
         // One thread loads Q and the K ring, another the V ring, so that a late K slot never
-        // holds back a V load.  Every fourth query pair of a head also prefetches the tiles
-        // PREFETCH_TILES ahead into L2: the CTAs of one head walk the same keys in step, so
-        // without it every tile would be a DRAM-latency load, and one prefetching CTA in four
-        // is enough to keep the others hitting in L2.
+        // holds back a V load.
         if (lane == 0) {
             const bool is_k = (warp == TMA_WARP);
             const CUtensorMap* map = is_k ? &p.kmap[b] : &p.vmap[b];
@@ -206,9 +203,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                     for (int hf = 0; hf < 2; ++hf)
                         tma_load_3d(sQ + t * TILE + hf * HALF, qm, BAR(B_QFULL), hf * 64, q0 + t * BM, plane);
             }
-            const bool do_pf = (qp % 4) == 0;   // every fourth query pair prefetches
-            for (int j = 0; do_pf && j < PREFETCH_TILES && j < ntiles; ++j)
-                for (int hf = 0; hf < 2; ++hf) tma_prefetch_l2_3d(map, hf * 64, (t_begin + j) * BN, h);
             int pend[NST] = {};
             uint32_t par[NST] = {};
             for (int j = 0; j < ntiles; ++j) {
@@ -216,8 +210,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                 const uint32_t ph = static_cast<uint32_t>(j / nst) & 1u;
                 if (!mbar_wait_bounded(BAR(bar_empty + st), ph ^ 1u, tmo, abort_flag)) { raise_abort(abort_flag, p.err); break; }
                 const int jg = t_begin + j;
-                if (do_pf && j + PREFETCH_TILES < ntiles)
-                    for (int hf = 0; hf < 2; ++hf) tma_prefetch_l2_3d(map, hf * 64, (jg + PREFETCH_TILES) * BN, h);
                 if (jg != p.drop_tile) {
                     mbar_arrive_expect_tx(BAR(bar_full + st), TILE);
                     for (int hf = 0; hf < 2; ++hf)
