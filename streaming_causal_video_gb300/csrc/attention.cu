@@ -69,6 +69,7 @@ constexpr int TMA_V_WARP = 4 * NQT + 2;  // V tiles
 constexpr int NTHREADS = (4 * NQT + 3) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr float kFastSumBound = 256.0f;     // 2^kRescaleThreshold: largest row sum the optimistic pass accepts
 constexpr float kLn2 = 0.6931471805599453f;
 
 // barrier indices
@@ -323,66 +324,114 @@ __global__ void __launch_bounds__(NTHREADS, 1) chunk_attention_kernel(const __gr
                 for (int i = 0; i < 128; ++i)
                     if (i >= valid) r[i] = 0xFF800000u;       // -inf: masked key
             }
-            // Row max of the raw scores (scale > 0 commutes with max): 8 independent chains of
-            // three-input max, each over the 16 scores i = a (mod 8).
-            float mx8[8];
+            const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
+            bool done = false;
+            if (j > 0) {
+                // Optimistic pass: the exponentials against the running max, without this tile's
+                // max.  The running max is raised only when a tile's scores exceed it by more than
+                // 2^8 (lazy rescale below), which is exactly when some term of the pass would exceed
+                // 2^8; a row sum of at most 2^8 rules that out, and then the terms, the packed P and
+                // the sum (same four chains, same order as the pass below) are what the max pass
+                // would have produced.  Otherwise S, still intact in tensor memory, is loaded again
+                // for the max pass.
+                const uint64_t negm2 = f32x2_pack(-m_run, -m_run);
+                uint64_t sum4[4];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                float m = fmax3(__uint_as_float(r[a]), __uint_as_float(r[a + 8]), __uint_as_float(r[a + 16]));
+                for (int a2 = 0; a2 < 4; ++a2) sum4[a2] = 0;
+                uint32_t pk[2][32];
 #pragma unroll
-                for (int i = 24; i < 120; i += 16)
-                    m = fmax3(m, __uint_as_float(r[i + a]), __uint_as_float(r[i + 8 + a]));
-                mx8[a] = fmaxf(m, __uint_as_float(r[120 + a]));
-            }
-            const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-            const float m_new = fmaxf(m_run, mx * sl2);
-            const bool grow = m_new > m_run + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, grow)) {
-                const float f = grow ? ex2_approx(m_run - m_new) : 1.0f;
-                if (j > 0) {
-                    // O_t is stable here: S_t(j) was committed after O_t += P_t(j-1) V(j-1).
-#pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t o[32];
-                        tmem_ld_x32_sync(tO + c * 32, o);
+                for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-                        tmem_st_x32(tO + c * 32, o);
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = hf * 64 + 2 * i;
+                        const uint64_t x = ffma2(f32x2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sl2x2, negm2);
+                        float x0, x1;
+                        f32x2_unpack(x, x0, x1);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        sum4[i & 3] = fadd2(sum4[i & 3], f32x2_pack(p0, p1));
+                        pk[hf][i] = pack_bf16x2(p0, p1);
                     }
                 }
-                if (grow) {
-                    l_run *= f;
-                    m_run = m_new;
-                }
-            }
-            // p = 2^(s * scale * log2(e) - m): one packed FFMA per two scores, one MUFU.EX2 per
-            // score; the row sum accumulates pairs with packed adds in 4 independent chains.
-            const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
-            const uint64_t negm2 = f32x2_pack(-m_run, -m_run);
-            uint64_t sum4[4];
-#pragma unroll
-            for (int a = 0; a < 4; ++a) sum4[a] = 0;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int e = hf * 64 + 2 * i;
-                    const uint64_t x = ffma2(f32x2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sl2x2, negm2);
-                    float x0, x1;
-                    f32x2_unpack(x, x0, x1);
-                    const float p0 = ex2_approx(x0);
-                    const float p1 = ex2_approx(x1);
-                    sum4[i & 3] = fadd2(sum4[i & 3], f32x2_pack(p0, p1));
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st_x32(tS + hf * 32, pk);
-            }
-            {
                 const uint64_t s01 = fadd2(sum4[0], sum4[1]), s23 = fadd2(sum4[2], sum4[3]);
                 float lo, hi;
                 f32x2_unpack(fadd2(s01, s23), lo, hi);
-                l_run += lo + hi;
+                const float s_tile = lo + hi;
+                if (__all_sync(0xffffffffu, s_tile <= kFastSumBound)) {
+                    tmem_st_x32(tS, pk[0]);
+                    tmem_st_x32(tS + 32, pk[1]);
+                    l_run += s_tile;
+                    done = true;
+                } else {
+                    tmem_ld_x128_sync(tS, r);
+                    if (valid < BN) {
+#pragma unroll
+                        for (int i = 0; i < 128; ++i)
+                            if (i >= valid) r[i] = 0xFF800000u;
+                    }
+                }
+            }
+            if (!done) {
+                // Row max of the raw scores (scale > 0 commutes with max): 8 independent chains of
+                // three-input max, each over the 16 scores i = a (mod 8).
+                float mx8[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) {
+                    float m = fmax3(__uint_as_float(r[a]), __uint_as_float(r[a + 8]), __uint_as_float(r[a + 16]));
+#pragma unroll
+                    for (int i = 24; i < 120; i += 16)
+                        m = fmax3(m, __uint_as_float(r[i + a]), __uint_as_float(r[i + 8 + a]));
+                    mx8[a] = fmaxf(m, __uint_as_float(r[120 + a]));
+                }
+                const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+                const float m_new = fmaxf(m_run, mx * sl2);
+                const bool grow = m_new > m_run + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float f = grow ? ex2_approx(m_run - m_new) : 1.0f;
+                    if (j > 0) {
+                        // O_t is stable here: S_t(j) was committed after O_t += P_t(j-1) V(j-1).
+#pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t o[32];
+                            tmem_ld_x32_sync(tO + c * 32, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                            tmem_st_x32(tO + c * 32, o);
+                        }
+                    }
+                    if (grow) {
+                        l_run *= f;
+                        m_run = m_new;
+                    }
+                }
+                // p = 2^(s * scale * log2(e) - m): one packed FFMA per two scores, one MUFU.EX2 per
+                // score; the row sum accumulates pairs with packed adds in 4 independent chains.
+                const uint64_t negm2 = f32x2_pack(-m_run, -m_run);
+                uint64_t sum4[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) sum4[a] = 0;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = hf * 64 + 2 * i;
+                        const uint64_t x = ffma2(f32x2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sl2x2, negm2);
+                        float x0, x1;
+                        f32x2_unpack(x, x0, x1);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        sum4[i & 3] = fadd2(sum4[i & 3], f32x2_pack(p0, p1));
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st_x32(tS + hf * 32, pk);
+                }
+                {
+                    const uint64_t s01 = fadd2(sum4[0], sum4[1]), s23 = fadd2(sum4[2], sum4[3]);
+                    float lo, hi;
+                    f32x2_unpack(fadd2(s01, s23), lo, hi);
+                    l_run += lo + hi;
+                }
             }
             tmem_wait_st();
             tc_fence_before();
