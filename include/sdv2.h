@@ -91,7 +91,8 @@ typedef struct {
 /* ---- sizes ------------------------------------------------------------------------------ */
 
 /* Bytes of the workspace: a header with the device error word, the fp32 cos/sin tables of the
- * h and w axes, and the attention's key-split scratch (per-item arrival counters, per-row
+ * h and w axes (position-major for the append kernel and a pair-major copy for the fused
+ * projection), and the attention's key-split scratch (per-item arrival counters, per-row
  * running max and sum, per-row unnormalised fp32 outputs for up to 4 key splits of every
  * (stream, head, 256 query rows) item).  The workspace belongs to one configuration; it may
  * be shared by all layers, but calls that use it must not overlap on the GPU (use one
@@ -112,7 +113,7 @@ int64_t sdv2_visible_tokens(const sdv2_stream_cfg* cfg, int64_t chunk_index);
 /* ---- set-up ----------------------------------------------------------------------------- */
 
 /* Fill the workspace: zero it, then write the header and the fp32 cos/sin tables of the h and
- * w axes (angles and cos/sin in fp64 on the host, rounded once to fp32).  Enqueues a memset
+ * w axes in both layouts (angles and cos/sin in fp64 on the host, rounded once to fp32).  Enqueues a memset
  * and copies on `stream` and synchronizes it before returning.
  * ws: device, sdv2_workspace_bytes(cfg) bytes. */
 sdv2_status sdv2_workspace_init(const sdv2_stream_cfg* cfg, void* ws, void* stream);

@@ -173,9 +173,10 @@ sdv2_status cuda_status(cudaError_t e, const char* what)
     return fail(SDV2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// Workspace: [error word | h table | w table | split counters | split (m, l) | split rows].
+// Workspace: [error word | h table | w table | h table, pair-major | w table, pair-major |
+// split counters | split (m, l) | split rows].
 struct WsLayout {
-    size_t htab, wtab, counters, part_ml, part_o, total;
+    size_t htab, wtab, htab_pm, wtab_pm, counters, part_ml, part_o, total;
 };
 
 WsLayout ws_layout(const sdv2_stream_cfg* c)
@@ -189,6 +190,10 @@ WsLayout ws_layout(const sdv2_stream_cfg* c)
     L.htab = off;
     off += round_up(sizeof(float2) * c->grid_h * (c->rope_h / 2), 256);
     L.wtab = off;
+    off += round_up(sizeof(float2) * c->grid_w * (c->rope_w / 2), 256);
+    L.htab_pm = off;
+    off += round_up(sizeof(float2) * c->grid_h * (c->rope_h / 2), 256);
+    L.wtab_pm = off;
     off += round_up(sizeof(float2) * c->grid_w * (c->rope_w / 2), 256);
     L.counters = off;
     off += round_up(sizeof(int32_t) * 2 * items, 256);       // tickets, published splits
@@ -276,11 +281,21 @@ sdv2_status sdv2_workspace_init(const sdv2_stream_cfg* c, void* ws, void* stream
     if (!ws || !aligned16(ws)) return fail(SDV2_ERR_INVALID_ARG, "ws must be a non-null 16-byte aligned pointer");
     if ((s = check_device()) != SDV2_OK) return s;
     const WsLayout L = ws_layout(c);
-    std::vector<float> htab(2 * c->grid_h * (c->rope_h / 2)), wtab(2 * c->grid_w * (c->rope_w / 2));
+    const int hp = c->rope_h / 2, wp = c->rope_w / 2;
+    std::vector<float> htab(2 * c->grid_h * hp), wtab(2 * c->grid_w * wp);
+    std::vector<float> htab_pm(htab.size()), wtab_pm(wtab.size());     // [pair][position]
     for (int y = 0; y < c->grid_h; ++y)
-        for (int j = 0; j < c->rope_h / 2; ++j) cos_sin_f32(y, j, c->rope_h, c->rope_base, &htab[2 * (y * (c->rope_h / 2) + j)]);
+        for (int j = 0; j < hp; ++j) {
+            cos_sin_f32(y, j, c->rope_h, c->rope_base, &htab[2 * (y * hp + j)]);
+            htab_pm[2 * (j * c->grid_h + y)] = htab[2 * (y * hp + j)];
+            htab_pm[2 * (j * c->grid_h + y) + 1] = htab[2 * (y * hp + j) + 1];
+        }
     for (int x = 0; x < c->grid_w; ++x)
-        for (int j = 0; j < c->rope_w / 2; ++j) cos_sin_f32(x, j, c->rope_w, c->rope_base, &wtab[2 * (x * (c->rope_w / 2) + j)]);
+        for (int j = 0; j < wp; ++j) {
+            cos_sin_f32(x, j, c->rope_w, c->rope_base, &wtab[2 * (x * wp + j)]);
+            wtab_pm[2 * (j * c->grid_w + x)] = wtab[2 * (x * wp + j)];
+            wtab_pm[2 * (j * c->grid_w + x) + 1] = wtab[2 * (x * wp + j) + 1];
+        }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned char* base = static_cast<unsigned char*>(ws);
     cudaError_t e = cudaMemsetAsync(ws, 0, L.total, st);
@@ -288,6 +303,10 @@ sdv2_status sdv2_workspace_init(const sdv2_stream_cfg* c, void* ws, void* stream
         e = cudaMemcpyAsync(base + L.htab, htab.data(), htab.size() * sizeof(float), cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess && !wtab.empty())
         e = cudaMemcpyAsync(base + L.wtab, wtab.data(), wtab.size() * sizeof(float), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && !htab_pm.empty())
+        e = cudaMemcpyAsync(base + L.htab_pm, htab_pm.data(), htab_pm.size() * sizeof(float), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && !wtab_pm.empty())
+        e = cudaMemcpyAsync(base + L.wtab_pm, wtab_pm.data(), wtab_pm.size() * sizeof(float), cudaMemcpyHostToDevice, st);
     WsHeader hdr{0, 0, L.counters, L.part_ml - L.counters};
     if (e == cudaSuccess) e = cudaMemcpyAsync(ws, &hdr, sizeof(hdr), cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -428,8 +447,8 @@ sdv2_status sdv2_qkv_rope_append(const sdv2_stream_cfg* c, const int64_t* start_
     p.k_cache = static_cast<uint16_t*>(k_cache);
     p.v_cache = static_cast<uint16_t*>(v_cache);
     p.meta = static_cast<sdv2_slot_meta*>(meta);
-    p.h_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + L.htab);
-    p.w_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + L.wtab);
+    p.h_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + L.htab_pm);
+    p.w_tab = reinterpret_cast<const float2*>(static_cast<const unsigned char*>(ws) + L.wtab_pm);
     p.err = static_cast<uint32_t*>(ws);
     p.timeout_ns = g_timeout_ns.load();
     p.M = static_cast<int32_t>(M);
@@ -437,6 +456,7 @@ sdv2_status sdv2_qkv_rope_append(const sdv2_stream_cfg* c, const int64_t* start_
     p.B = c->batch;
     p.H = c->heads;
     p.HW = static_cast<int32_t>(hw_of(c));
+    p.grid_h = c->grid_h;
     p.grid_w = c->grid_w;
     p.F = c->chunk_frames;
     p.nslots = static_cast<int32_t>(slots_of(c));

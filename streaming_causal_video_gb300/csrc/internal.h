@@ -158,11 +158,11 @@ struct QkvRopeParams {
     uint16_t* k_cache;
     uint16_t* v_cache;
     sdv2_slot_meta* meta;
-    const float2* h_tab;
-    const float2* w_tab;
+    const float2* h_tab;                      // pair-major: [rope_h/2][grid_h] (cos, sin)
+    const float2* w_tab;                      // pair-major: [rope_w/2][grid_w]
     uint32_t* err;
     uint64_t timeout_ns;
-    int32_t M, C, B, H, HW, grid_w, F, nslots, Nq;
+    int32_t M, C, B, H, HW, grid_h, grid_w, F, nslots, Nq;
     int32_t tp, hp, wp;
     FrameDesc frames[kMaxChunkFrames];
     float2 tcs[kMaxTimePairs];

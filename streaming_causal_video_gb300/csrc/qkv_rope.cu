@@ -9,26 +9,32 @@
 // frame and chunk, as in sdv2_rope_append_kv) and writes q_rot (head-major) and k_rot, v into
 // the frames' cache slots, without a round trip of q, k, v through memory.
 //
-// Tiling: persistent CTAs, one per SM, walk the tiles of 128 tokens x 192 features (tile t,
-// t + gridDim.x, ...; the constants also allow two 128-row halves per tile).  A tile's fp32
-// accumulator takes 256 of the 512 tensor-memory columns, so two tiles fit: the MMA warp fills
-// one accumulator buffer while the epilogue drains the other, and the epilogue of a tile runs
-// under the next tile's main loop.  The hidden dimension streams in steps of 64 (128-byte
-// swizzled TMA boxes) through a 4-stage ring of 40 KB stages.  N = 192 MMAs read their
-// operands from shared memory at 107 bytes per cycle (a 256 x 128 tile as two M = 128 halves
-// needs 128, the whole shared-memory bandwidth), and 4680 x 4608 makes 888 tiles, 5.84 per SM
-// (128 x 256: 666 tiles, 4.38 per SM, 5 on some).  A tile may straddle heads and the q|k|v
-// boundaries (the epilogue finds the type and head of each 32-feature chunk); the last feature
-// tile may be ragged (its weight rows past the end load as zeros and the epilogue skips them).
-//   warp 0: TMA producer; warp 1: MMA issuer (converged: every lane polls the stage barrier and
-//   a warp vote agrees on the outcome; elect.sync issues); warps 2-9: epilogue, two per TMEM lane
-//   quarter (one per half), thread = token row, with the next 32-column TMEM load in flight while
-//   the current chunk is rotated and stored (bias read as float4); with one 128-row half the two
-//   warps of a quarter take the two halves of the columns.  A chunk's 16 cos/sin pairs
-//   are loaded into registers before any is used: each pair's table (time, h or w axis) is
-//   picked by a pointer select, so the 16 loads issue back to back instead of one per branch
-//   of the axis test.  Barriers: full/empty per ring stage; accumulator full/empty per buffer
-//   (the empty one counts the eight epilogue warps).
+// Tiling: clusters of two CTAs on the two SMs of a TPC share each MMA (tcgen05.mma.cta_group::2,
+// M = 256): a pair tile is 256 tokens x 192 features; each CTA holds its 128 token rows and
+// half of the 192 weight rows per hidden step, and the accumulator of its 128 rows x 192
+// features lands in its own tensor memory.  Each SM stages 28 KB per hidden step of 64 instead
+// of the 40 KB a 128 x 192 tile on one SM needs, so a 6-stage ring (168 KB) keeps enough copies
+// in flight and still leaves ~60 KB of L1 for the epilogue's table reads.  4680 x 4608 makes
+// 19 x 24 = 456 pair tiles, 6 per pair on 76 pairs.  Pairs are persistent (tile t, t + pairs,
+// ...); a CTA's fp32 accumulator takes 192 of the 256 columns of a tensor-memory buffer, so two
+// tiles fit: the MMA warp fills one buffer while the epilogues of both CTAs drain the other.
+// A tile may straddle heads and the q|k|v boundaries (the epilogue finds the type and head of
+// each 32-feature chunk); rows past the last token and feature rows past 3*H*D load as zeros
+// and the epilogue skips them.
+//   warp 0: TMA producer (both CTAs load into their own shared memory and count the bytes on
+//   the leader CTA's stage barrier; the leader arms it for both); warp 1: in the leader, MMA
+//   issuer (converged: every lane polls, a warp vote agrees; elect.sync issues), whose commits
+//   arrive on the barriers of both CTAs; warps 2-9: epilogue, two per TMEM lane quarter (each
+//   takes half of the columns), thread = token row, with the next 32-column TMEM load in flight
+//   while the current chunk is rotated and stored (bias read as float4), arriving on the
+//   leader's accumulator-empty barrier (sixteen warps over the pair) when a buffer is drained.
+// The epilogue is what bounds this kernel (the MMA loop alone runs at the speed of a library
+// GEMM of the same shape), and its cost is the number of distinct rows each warp instruction
+// touches: a chunk's 16 cos/sin pairs come from pair-major copies of the h and w tables, where
+// the warp's consecutive tokens read adjacent entries, each from a pointer picked by select so
+// that the 16 loads issue back to back; and the four lanes of each quad transpose their 64-byte
+// row segments with two xor-shuffle steps, so each store instruction writes 8 whole segments
+// instead of 16 bytes of 32 rows.
 // Rounding: acc (fp32, fp32 accumulation) + bias (fp32 add); q and k pairs rotated in fp32 as
 // (fmaf(x, c, -(y*s)), fmaf(x, s, y*c)); one bf16 round-to-nearest-even per output.
 #include <cuda_bf16.h>
@@ -38,29 +44,30 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "ptx_pair.cuh"
 
 namespace sdv2 {
 namespace {
 
-constexpr int QBM = 128;                       // tokens per tile: 1 or 2 halves of 128 rows
-constexpr int QBN = 192;                       // features per tile
-constexpr int QHALVES = QBM / 128;             // 128-row accumulators per tile
-static_assert((QHALVES == 1 || QHALVES == 2) && QHALVES * QBN <= 256 && QBN % 64 == 0 && QBN <= 256,
-              "a tile's accumulators fit in one 256-column buffer; the epilogue splits them in 32-column chunks");
+constexpr int PBM = 256;                       // tokens per pair tile
+constexpr int PBN = 192;                       // features per pair tile
+constexpr int CBM = PBM / 2;                   // token rows in each CTA
+constexpr int CBN = PBN / 2;                   // weight rows in each CTA
+static_assert(PBN % 64 == 0 && PBN <= 256, "N of an M = 256 pair MMA; the epilogue splits it in 32-column chunks per half");
 constexpr int QBK = 64;                        // hidden elements per step (128 bytes of bf16)
-constexpr int QST = 4;                         // ring stages
-constexpr uint32_t A_BYTES = QBM * QBK * 2;    // 32 KB
-constexpr uint32_t A_HALF = A_BYTES / 2;       // rows 128..255 of the A box start here
-constexpr uint32_t B_BYTES = QBN * QBK * 2;    // 16 KB
+constexpr int QST = 6;                         // ring stages
+constexpr uint32_t A_BYTES = CBM * QBK * 2;    // 16 KB
+constexpr uint32_t B_BYTES = CBN * QBK * 2;    // 12 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int QTHREADS = 10 * 32;
 constexpr int QEPI_WARPS = 8;
-constexpr uint32_t QACC_COLS = 256;            // accumulator buffer stride: QHALVES halves of QBN columns each
+constexpr uint32_t QACC_COLS = 256;            // accumulator buffer stride
 constexpr uint32_t QTMEM_COLS = 512;           // two accumulator buffers, at columns 0 and 256
 // barriers: full[QST], empty[QST], acc_full[2], acc_empty[2], mma_done
 constexpr int QB_FULL = 0, QB_EMPTY = QST, QB_ACC_FULL = 2 * QST, QB_ACC_EMPTY = 2 * QST + 2,
               QB_DONE = 2 * QST + 4, QNBARS = 2 * QST + 5;
 constexpr uint32_t QSMEM_BYTES = QST * STAGE_BYTES + 256 + 1024;
+constexpr uint16_t kBothCtas = 0x3;
 static_assert(QNBARS * 8 + 8 <= 256, "barriers and flags fit their 256 bytes");
 static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "128-byte swizzle needs 1024-byte aligned tiles");
 static_assert(QSMEM_BYTES <= 232448, "shared memory per CTA");
@@ -91,6 +98,15 @@ __device__ __forceinline__ void tmem_wait_ld_tied(uint32_t (&r)[32])
                  : "memory");
 }
 
+__device__ __forceinline__ uint4 shfl_xor_u4(uint4 v, int mask)
+{
+    v.x = __shfl_xor_sync(0xffffffffu, v.x, mask);
+    v.y = __shfl_xor_sync(0xffffffffu, v.y, mask);
+    v.z = __shfl_xor_sync(0xffffffffu, v.z, mask);
+    v.w = __shfl_xor_sync(0xffffffffu, v.w, mask);
+    return v;
+}
+
 __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_constant__ QkvRopeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -103,10 +119,12 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
 #define QBAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
     const int lane = threadIdx.x & 31;
-    const int ntn = (3 * p.H * 128 + QBN - 1) / QBN;        // feature tiles (the last may be ragged)
-    const int ntiles = ((p.M + QBM - 1) / QBM) * ntn;
-    const int my_tiles = static_cast<int>(blockIdx.x) < ntiles
-                             ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
+    const uint32_t rank = cluster_ctarank();                 // 0: the leader, which issues the MMAs
+    const int pair = static_cast<int>(cluster_id_x());
+    const int npairs = static_cast<int>(cluster_count_x());
+    const int ntn = (3 * p.H * 128 + PBN - 1) / PBN;        // feature tiles (the last may be ragged)
+    const int ntiles = ((p.M + PBM - 1) / PBM) * ntn;
+    const int my_tiles = pair < ntiles ? (ntiles - 1 - pair) / npairs + 1 : 0;
     const int ksteps = p.C / QBK;
     const uint64_t tmo = p.timeout_ns;
 
@@ -117,129 +135,133 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(QBAR(QB_ACC_FULL + i), 1);
-            mbar_init(QBAR(QB_ACC_EMPTY + i), QEPI_WARPS);
+            mbar_init(QBAR(QB_ACC_EMPTY + i), 2 * QEPI_WARPS);
         }
         mbar_init(QBAR(QB_DONE), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), QTMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(smem_u32(tmem_slot), QTMEM_COLS);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();          // both CTAs' barriers are initialised before either signals the other's
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ producer (both CTAs)
         if (lane == 0) {
             tma_prefetch_desc(&p.xmap);
             tma_prefetch_desc(&p.wmap);
-            int pend[QST] = {};
-            uint32_t par[QST] = {};
+            const uint32_t full_leader = map_to_rank(QBAR(QB_FULL), 0);
+            uint32_t pend = 0, par = 0;                      // per stage: armed, and the parity it was armed in
             bool ok = true;
             int g = 0;                                       // k-steps issued so far, over all tiles
             for (int li = 0; ok && li < my_tiles; ++li) {
-                const int tile = static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x);
-                const int m0 = (tile / ntn) * QBM;
-                const int n0 = (tile % ntn) * QBN;
+                const int tile = pair + li * npairs;
+                const int m0 = (tile / ntn) * PBM + static_cast<int>(rank) * CBM;
+                const int n0 = (tile % ntn) * PBN + static_cast<int>(rank) * CBN;
                 for (int kk = 0; kk < ksteps; ++kk, ++g) {
                     const int st = g % QST;
                     const uint32_t ph = static_cast<uint32_t>(g / QST) & 1u;
-                    if (!mbar_wait_bounded(QBAR(QB_EMPTY + st), ph ^ 1u, tmo, abort_flag)) {
+                    // the leader's commit of the stage's previous MMAs arrives on both CTAs' barrier
+                    if (!mbar_wait_cluster_bounded(QBAR(QB_EMPTY + st), ph ^ 1u, tmo, abort_flag)) {
                         *abort_flag = 1;
                         atomicOr(p.err, kErrTimeout);
                         ok = false;
                         break;
                     }
                     const uint32_t sa = s0 + st * STAGE_BYTES;
-                    mbar_arrive_expect_tx(QBAR(QB_FULL + st), STAGE_BYTES);
-                    tma_load_3d(sa, &p.xmap, QBAR(QB_FULL + st), kk * QBK, m0, 0);
-                    tma_load_3d(sa + A_BYTES, &p.wmap, QBAR(QB_FULL + st), kk * QBK, n0, 0);
-                    pend[st] = 1;
-                    par[st] = ph;
+                    if (rank == 0) mbar_arrive_expect_tx(QBAR(QB_FULL + st), 2 * STAGE_BYTES);
+                    const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(st);
+                    tma_load_3d_pair(sa, &p.xmap, fb, kk * QBK, m0, 0);
+                    tma_load_3d_pair(sa + A_BYTES, &p.wmap, fb, kk * QBK, n0, 0);
+                    pend |= 1u << st;
+                    par = (par & ~(1u << st)) | (ph << st);
                 }
             }
-            // Drain: the last copy into each stage must land before the CTA may exit (earlier
-            // ones were consumed by the MMA warp before the stage was refilled).
-            volatile int no_abort = 0;
-            for (int i = 0; i < QST; ++i)
-                if (pend[i]) mbar_wait_bounded(QBAR(QB_FULL + i), par[i], tmo, &no_abort);
+            // Drain (leader): the last copies into each stage, its own and the peer's, must land
+            // before the pair may exit (earlier ones were consumed by the MMAs before the stage
+            // was refilled).  The peer stays resident until then: both CTAs meet at the final
+            // cluster barrier.
+            if (rank == 0) {
+                volatile int no_abort = 0;
+                for (int i = 0; i < QST; ++i)
+                    if ((pend >> i) & 1u) mbar_wait_cluster_bounded(QBAR(QB_FULL + i), (par >> i) & 1u, tmo, &no_abort);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_bf16_f32(128, QBN, false);
-        const uint64_t dA = sdesc_sw128(s0, 16, 1024);
-        const uint64_t dB = sdesc_sw128(s0 + A_BYTES, 16, 1024);
-        constexpr uint64_t kStage = STAGE_BYTES >> 4;
-        constexpr uint64_t kHalf = A_HALF >> 4;
-        auto wait = [&](int bar_idx, uint32_t parity) -> bool {
-            const bool r = mbar_wait_bounded(QBAR(bar_idx), parity, tmo, abort_flag);
-            return __all_sync(0xffffffffu, r);
-        };
-        bool ok = true;
-        int g = 0;
-        for (int li = 0; ok && li < my_tiles; ++li) {
-            const int buf = li & 1;
-            // the epilogue has drained this buffer's previous tile (first use: passes at once)
-            if (!wait(QB_ACC_EMPTY + buf, (static_cast<uint32_t>(li >> 1) & 1u) ^ 1u)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t dacc = tmem + static_cast<uint32_t>(buf) * QACC_COLS;
-            for (int kk = 0; kk < ksteps; ++kk, ++g) {
-                const int st = g % QST;
-                if (!wait(QB_FULL + st, static_cast<uint32_t>(g / QST) & 1u)) {
+        if (rank == 0) {
+            // -------------------------------------------------------- MMA issuer (leader)
+            constexpr uint32_t idesc = idesc_bf16_f32(PBM, PBN, false);
+            const uint64_t dA = sdesc_sw128(s0, 16, 1024);
+            const uint64_t dB = sdesc_sw128(s0 + A_BYTES, 16, 1024);
+            constexpr uint64_t kStage = STAGE_BYTES >> 4;
+            auto wait = [&](int bar_idx, uint32_t parity) -> bool {
+                const bool r = mbar_wait_cluster_bounded(QBAR(bar_idx), parity, tmo, abort_flag);
+                return __all_sync(0xffffffffu, r);
+            };
+            bool ok = true;
+            int g = 0;
+            for (int li = 0; ok && li < my_tiles; ++li) {
+                const int buf = li & 1;
+                // both CTAs' epilogues have drained this buffer's previous tile (first use: passes at once)
+                if (!wait(QB_ACC_EMPTY + buf, (static_cast<uint32_t>(li >> 1) & 1u) ^ 1u)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t a = dA + static_cast<uint64_t>(st) * kStage;
-                const uint64_t b = dB + static_cast<uint64_t>(st) * kStage;
-                // both halves of the tile multiply the same weight stage
-#pragma unroll
-                for (int hh = 0; hh < QHALVES; ++hh)
+                const uint32_t dacc = tmem + static_cast<uint32_t>(buf) * QACC_COLS;
+                for (int kk = 0; kk < ksteps; ++kk, ++g) {
+                    const int st = g % QST;
+                    if (!wait(QB_FULL + st, static_cast<uint32_t>(g / QST) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a = dA + static_cast<uint64_t>(st) * kStage;
+                    const uint64_t b = dB + static_cast<uint64_t>(st) * kStage;
 #pragma unroll
                     for (int k = 0; k < QBK / 16; ++k)
-                        mma_ss_warp(dacc + static_cast<uint32_t>(hh * QBN),
-                                    a + static_cast<uint64_t>(hh) * kHalf + static_cast<uint64_t>(k * 2),
-                                    b + static_cast<uint64_t>(k * 2), idesc, (kk > 0 || k > 0) ? 1u : 0u);
-                mma_commit_warp(QBAR(QB_EMPTY + st));
+                        mma_ss_pair_warp(dacc, a + static_cast<uint64_t>(k * 2), b + static_cast<uint64_t>(k * 2), idesc,
+                                         (kk > 0 || k > 0) ? 1u : 0u);
+                    mma_commit_pair_warp(QBAR(QB_EMPTY + st), kBothCtas);
+                }
+                if (!ok) break;
+                mma_commit_pair_warp(QBAR(QB_ACC_FULL + buf), kBothCtas);   // this tile's accumulators are complete
             }
-            if (!ok) break;
-            mma_commit_warp(QBAR(QB_ACC_FULL + buf));        // this tile's accumulators are complete
+            if (!ok && lane == 0) {
+                *abort_flag = 1;
+                atomicOr(p.err, kErrTimeout);
+            }
+            // Tensor memory of both CTAs is freed only after every MMA has completed.
+            mma_commit_pair_warp(QBAR(QB_DONE), kBothCtas);
         }
-        if (!ok && lane == 0) {
-            *abort_flag = 1;
-            atomicOr(p.err, kErrTimeout);
-        }
-        // Tensor memory is freed only after every MMA of this warp has completed.
-        mma_commit_warp(QBAR(QB_DONE));
         if (lane == 0) {
             volatile int no_abort = 0;
-            mbar_wait_bounded(QBAR(QB_DONE), 0, tmo, &no_abort);
+            mbar_wait_cluster_bounded(QBAR(QB_DONE), 0, tmo, &no_abort);
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ epilogue: 256 threads
+        // ------------------------------------------------------------ epilogue: 256 threads per CTA
         // Two warps per TMEM lane quarter (a warp reaches the lanes of quarter warp index mod 4):
-        // with two 128-row halves, warps 2-5 read rows 0..127 and warps 6-9 rows 128..255, all
-        // columns; with one half, warps 2-5 read the first half of the columns, warps 6-9 the
-        // second.  Either way a thread drains 128 columns of one row.
+        // warps 2-5 drain the first half of the columns, warps 6-9 the second; thread = token row.
         const int part = (warp - 2) >> 2;
         const int quarter = warp & 3;
-        const int row = (QHALVES == 2 ? part * 128 : 0) + quarter * 32 + lane;
-        const int col0 = QHALVES == 2 ? 0 : part * (QBN / 2);          // first column (feature) of this thread
-        constexpr int kEpiCols = QBN * QHALVES / 2;                    // columns one thread drains
+        const int row = quarter * 32 + lane;
+        const int col0 = part * (PBN / 2);                               // first column (feature) of this thread
+        constexpr int kEpiCols = PBN / 2;                                // columns one thread drains
         const int hd = p.H * 128;
         const int64_t rows = static_cast<int64_t>(p.nslots) * p.HW;
+        const uint32_t acc_empty_leader = map_to_rank(QBAR(QB_ACC_EMPTY), 0);
         for (int li = 0; li < my_tiles; ++li) {
             const int buf = li & 1;
-            bool ok = mbar_wait_bounded(QBAR(QB_ACC_FULL + buf), static_cast<uint32_t>(li >> 1) & 1u, tmo, abort_flag) &&
+            bool ok = mbar_wait_cluster_bounded(QBAR(QB_ACC_FULL + buf), static_cast<uint32_t>(li >> 1) & 1u, tmo,
+                                                abort_flag) &&
                       !*abort_flag;
             ok = __all_sync(0xffffffffu, ok);               // the TMEM loads below are warp-collective
             if (!ok) {
@@ -250,12 +272,11 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                 break;
             }
             tc_fence_after();
-            const int tile = static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x);
-            const int m0 = (tile / ntn) * QBM;
-            const int n0 = (tile % ntn) * QBN;
+            const int tile = pair + li * npairs;
+            const int m0 = (tile / ntn) * PBM + static_cast<int>(rank) * CBM;
+            const int n0 = (tile % ntn) * PBN;
             const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                  static_cast<uint32_t>(buf) * QACC_COLS +
-                                  static_cast<uint32_t>(QHALVES == 2 ? part * QBN : col0);
+                                  static_cast<uint32_t>(buf) * QACC_COLS + static_cast<uint32_t>(col0);
             const int m = m0 + row;
             const bool valid = m < p.M;
             const int mm = valid ? m : 0;
@@ -267,8 +288,14 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
             const int gw = r - gh * p.grid_w;
             const FrameDesc fd = p.frames[b * p.F + i];
             const float2* t_row = p.tcs + (b * p.F + i) * p.tp;
-            const float2* h_row = p.h_tab + gh * p.hp;
-            const float2* w_row = p.w_tab + gw * p.wp;
+            const float2* h_col = p.h_tab + gh;           // pair-major tables: the warp's consecutive
+            const float2* w_col = p.w_tab + gw;           // tokens read adjacent entries of a pair's row
+            // element offsets of this token's q_rot row and k/v cache row (head 0, dim 0)
+            const int64_t off_q = (static_cast<int64_t>(b) * p.H * p.Nq + n) * 128;
+            const int64_t off_kv = (static_cast<int64_t>(b) * p.H * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128;
+            const uint32_t valid_mask = __ballot_sync(0xffffffffu, valid);
+            const int quad0 = lane & ~3;                  // first lane of this thread's lane quad
+            const int qj = lane & 3;
             // the next chunk's TMEM load is in flight while this chunk is rotated and stored
             uint32_t a[2][32];
             tmem_ld_x32_async(trow, a[0]);
@@ -279,15 +306,14 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                 if (cchunk + 1 < kEpiCols / 32)
                     tmem_ld_x32_async(trow + static_cast<uint32_t>((cchunk + 1) * 32), a[(cchunk + 1) & 1]);
                 const int f0 = n0 + col0 + cchunk * 32;           // feature of cur[0]
-                if (valid && f0 < 3 * hd) {                       // features past 3*H*D: zero-filled weight rows
+                if (f0 < 3 * hd) {                                // features past 3*H*D: zero-filled weight rows
                     const int type = f0 / hd;                     // 0 = q, 1 = k, 2 = v
                     const int fl = f0 - type * hd;
                     const int head = fl >> 7;
                     const int d0 = fl & 127;                      // first dim of the chunk in its head
-                    const int64_t bh = static_cast<int64_t>(b) * p.H + head;
-                    uint16_t* dst = (type == 0) ? p.q_rot + (bh * p.Nq + n) * 128 + d0
-                                  : (type == 1) ? p.k_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0
-                                                : p.v_cache + (bh * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128 + d0;
+                    uint16_t* base = (type == 0) ? p.q_rot + static_cast<int64_t>(head) * p.Nq * 128 + d0
+                                   : ((type == 1) ? p.k_cache : p.v_cache) + static_cast<int64_t>(head) * rows * 128 + d0;
+                    const int64_t off = type == 0 ? off_q : off_kv;
                     float bv[32];
                     if (p.bias) {
                         const float4* b4 = reinterpret_cast<const float4*>(p.bias + f0);
@@ -306,7 +332,8 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                         for (int u = 0; u < 16; ++u) {
                             const int pr = (d0 >> 1) + u;
                             const float2* src = pr < p.tp ? t_row + pr
-                                              : pr < p.tp + p.hp ? h_row + (pr - p.tp) : w_row + (pr - p.tp - p.hp);
+                                              : pr < p.tp + p.hp ? h_col + (pr - p.tp) * p.grid_h
+                                                                 : w_col + (pr - p.tp - p.hp) * p.grid_w;
                             csv[u] = *src;           // generic load: t pairs live in the launch parameters
                         }
                     }
@@ -328,10 +355,30 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                         }
                         o[u] = pack2(x, y);
                     }
-                    uint4* d4 = reinterpret_cast<uint4*>(dst);
+                    // Lane quad transpose: lane j of a quad holds its token's 64-byte segment as
+                    // vectors e[0..3]; afterwards it holds vector j of the quad's four tokens, so
+                    // that each store below writes four whole segments (8 per warp) instead of a
+                    // sixteenth of 32 rows.  Step 1 swaps 2x2 blocks between lanes j and j^2,
+                    // step 2 the off-diagonal vectors of each block between lanes j and j^1.
+                    uint4 e[4];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-                    if (type == 1 && head == 0 && d0 == 0 && r == 0) {    // one writer per (stream, frame)
+                    for (int v = 0; v < 4; ++v) e[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+                    {
+                        const bool hi = (qj & 2) != 0;
+                        const uint4 s0 = hi ? e[0] : e[2], s1 = hi ? e[1] : e[3];
+                        const uint4 r0 = shfl_xor_u4(s0, 2), r1 = shfl_xor_u4(s1, 2);
+                        if (hi) { e[0] = r0; e[1] = r1; } else { e[2] = r0; e[3] = r1; }
+                        const bool odd = (qj & 1) != 0;
+                        const uint4 t0 = odd ? e[0] : e[1], t1 = odd ? e[2] : e[3];
+                        const uint4 u0 = shfl_xor_u4(t0, 1), u1 = shfl_xor_u4(t1, 1);
+                        if (odd) { e[0] = u0; e[2] = u1; } else { e[1] = u0; e[3] = u1; }
+                    }
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {                 // token quad0 + v, its vector qj
+                        const int64_t ov = __shfl_sync(0xffffffffu, off, quad0 + v);
+                        if ((valid_mask >> (quad0 + v)) & 1u) reinterpret_cast<uint4*>(base + ov)[qj] = e[v];
+                    }
+                    if (valid && type == 1 && head == 0 && d0 == 0 && r == 0) {    // one writer per (stream, frame)
                         sdv2_slot_meta md;
                         md.frame_id = fd.frame;
                         md.tpos = fd.tpos;
@@ -340,17 +387,18 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                 }
                 if (cchunk + 1 < kEpiCols / 32) tmem_wait_ld_tied(a[(cchunk + 1) & 1]);
             }
-            // every TMEM load of this buffer has completed: hand it back to the MMA warp
+            // every TMEM load of this buffer has completed: hand it back to the leader's MMA warp
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(QBAR(QB_ACC_EMPTY + buf));
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(buf));
         }
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();          // no CTA leaves while the other may still signal or read it
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, QTMEM_COLS);
+        tmem_dealloc_pair(tmem, QTMEM_COLS);
     }
 #undef QBAR
 }
@@ -394,28 +442,48 @@ bool encode_matrix(CUtensorMap* map, const void* base, int64_t rows, int64_t col
 cudaError_t launch_qkv_rope(QkvRopeParams& p, const void* x, const void* w, int64_t x_ld, cudaStream_t s,
                             const char** why)
 {
-    if (!encode_matrix(&p.xmap, x, p.M, p.C, x_ld, QBM) || !encode_matrix(&p.wmap, w, 3LL * p.H * 128, p.C, p.C, QBN)) {
+    if (!encode_matrix(&p.xmap, x, p.M, p.C, x_ld, CBM) || !encode_matrix(&p.wmap, w, 3LL * p.H * 128, p.C, p.C, CBN)) {
         *why = "cuTensorMapEncodeTiled failed for x or w_qkv";
         return cudaErrorInvalidValue;
     }
-    static std::atomic<uint64_t> attr_set{0};
     int dev = 0;
     cudaGetDevice(&dev);
-    const uint64_t bit = uint64_t(1) << (dev & 63);
-    if (!(attr_set.load() & bit)) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(QTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = QSMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // Per device, once: the shared-memory limit and how many CTA pairs can be resident at once
+    // (a persistent pair per TPC whose two SMs are both available).
+    static std::atomic<int> resident_pairs[64];
+    std::atomic<int>& slot = resident_pairs[dev & 63];
+    int pairs_max = slot.load();
+    if (pairs_max <= 0) {
         cudaError_t e = cudaFuncSetAttribute(qkv_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(QSMEM_BYTES));
         if (e != cudaSuccess) {
             *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
             return e;
         }
-        attr_set.fetch_or(bit);
+        e = cudaOccupancyMaxActiveClusters(&pairs_max, qkv_rope_kernel, &cfg);
+        if (e != cudaSuccess || pairs_max <= 0) {
+            *why = "no CTA pair of the fused projection kernel fits on this device";
+            return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+        }
+        slot.store(pairs_max);
     }
-    int sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t ntiles = static_cast<int64_t>((p.M + QBM - 1) / QBM) * ((3 * p.H * 128 + QBN - 1) / QBN);
-    const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(ntiles, std::max(1, sms))));
-    qkv_rope_kernel<<<grid, QTHREADS, QSMEM_BYTES, s>>>(p);
+    const int64_t ntiles = static_cast<int64_t>((p.M + PBM - 1) / PBM) * ((3 * p.H * 128 + PBN - 1) / PBN);
+    const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(ntiles, pairs_max));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, qkv_rope_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
