@@ -46,10 +46,12 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank)
     return r;
 }
 
-// Arrive (release at cluster scope) on a barrier given by its shared::cluster address.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+// Arrive on a barrier given by its shared::cluster address, with no memory ordering: for
+// signals whose only precondition is already complete in this thread (e.g. tensor-memory loads
+// finished by tcgen05.wait::ld), so that the arrival does not wait for earlier global stores.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // One poll of a local barrier, acquiring at cluster scope (its arrivals may come from the peer).

@@ -387,10 +387,12 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                 }
                 if (cchunk + 1 < kEpiCols / 32) tmem_wait_ld_tied(a[(cchunk + 1) & 1]);
             }
-            // every TMEM load of this buffer has completed: hand it back to the leader's MMA warp
+            // Every TMEM load of this buffer has completed (tcgen05.wait::ld above): hand it back
+            // to the leader's MMA warp.  The arrival orders nothing else, so it is relaxed: a
+            // release would first wait for this warp's global stores to reach cluster scope.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(buf));
+            if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader + 8u * static_cast<uint32_t>(buf));
         }
     }
     tc_fence_before();
