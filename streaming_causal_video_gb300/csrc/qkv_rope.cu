@@ -66,7 +66,15 @@ constexpr uint32_t QTMEM_COLS = 512;           // two accumulator buffers, at co
 // barriers: full[QST], empty[QST], acc_full[2], acc_empty[2], mma_done
 constexpr int QB_FULL = 0, QB_EMPTY = QST, QB_ACC_FULL = 2 * QST, QB_ACC_EMPTY = 2 * QST + 2,
               QB_DONE = 2 * QST + 4, QNBARS = 2 * QST + 5;
-constexpr uint32_t QSMEM_BYTES = QST * STAGE_BYTES + 256 + 1024;
+// Shared memory: [ring][cos/sin tables t | h | w, when they fit][bias of each epilogue warp's
+// columns of the current tile][barriers].  The 22 KB table area holds the tables of the 1.3B and
+// 14B 480p and the 720p shapes; larger tables are read from global memory.
+constexpr uint32_t TAB_OFF = QST * STAGE_BYTES;
+constexpr uint32_t TAB_BYTES = 22 * 1024;
+constexpr uint32_t BIAS_OFF = TAB_OFF + TAB_BYTES;
+constexpr uint32_t BIAS_BYTES = QEPI_WARPS * (PBN / 2) * 4;
+constexpr uint32_t BAR_OFF = BIAS_OFF + BIAS_BYTES;
+constexpr uint32_t QSMEM_BYTES = BAR_OFF + 256 + 1024;
 constexpr uint16_t kBothCtas = 0x3;
 static_assert(QNBARS * 8 + 8 <= 256, "barriers and flags fit their 256 bytes");
 static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "128-byte swizzle needs 1024-byte aligned tiles");
@@ -112,7 +120,7 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s0 = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QST * STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
     const uint32_t bar0 = smem_u32(bars);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + QNBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -258,6 +266,22 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
         const int hd = p.H * 128;
         const int64_t rows = static_cast<int64_t>(p.nslots) * p.HW;
         const uint32_t acc_empty_leader = map_to_rank(QBAR(QB_ACC_EMPTY), 0);
+        // The cos/sin tables go to shared memory once per CTA (while the first tile's MMAs run):
+        // read there, a chunk's 16 loads neither miss in L1 nor compete with the global stores.
+        const int n_t = p.B * p.F * p.tp, n_h = p.hp * p.grid_h, n_w = p.wp * p.grid_w;
+        const bool tabs_staged = static_cast<int64_t>(n_t + n_h + n_w) * 8 <= TAB_BYTES;
+        float2* tab_s = reinterpret_cast<float2*>(smem + TAB_OFF);
+        if (tabs_staged) {
+            const int et = static_cast<int>(threadIdx.x) - 64;
+            for (int k = et; k < n_t; k += 32 * QEPI_WARPS) tab_s[k] = p.tcs[k];
+            for (int k = et; k < n_h; k += 32 * QEPI_WARPS) tab_s[n_t + k] = p.h_tab[k];
+            for (int k = et; k < n_w; k += 32 * QEPI_WARPS) tab_s[n_t + n_h + k] = p.w_tab[k];
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * QEPI_WARPS) : "memory");    // the epilogue warps only
+        const float2* t_base = tabs_staged ? tab_s : p.tcs;
+        const float2* h_base = tabs_staged ? tab_s + n_t : p.h_tab;
+        const float2* w_base = tabs_staged ? tab_s + n_t + n_h : p.w_tab;
+        float* bias_w = reinterpret_cast<float*>(smem + BIAS_OFF) + (warp - 2) * (PBN / 2);
         for (int li = 0; li < my_tiles; ++li) {
             const int buf = li & 1;
             bool ok = mbar_wait_cluster_bounded(QBAR(QB_ACC_FULL + buf), static_cast<uint32_t>(li >> 1) & 1u, tmo,
@@ -287,9 +311,17 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
             const int gh = r / p.grid_w;
             const int gw = r - gh * p.grid_w;
             const FrameDesc fd = p.frames[b * p.F + i];
-            const float2* t_row = p.tcs + (b * p.F + i) * p.tp;
-            const float2* h_col = p.h_tab + gh;           // pair-major tables: the warp's consecutive
-            const float2* w_col = p.w_tab + gw;           // tokens read adjacent entries of a pair's row
+            const float2* t_row = t_base + (b * p.F + i) * p.tp;
+            const float2* h_col = h_base + gh;            // pair-major tables: the warp's consecutive
+            const float2* w_col = w_base + gw;            // tokens read adjacent entries of a pair's row
+            if (p.bias) {                                 // this warp's columns of the tile, one coalesced load each
+#pragma unroll
+                for (int j = 0; j < kEpiCols / 32; ++j) {
+                    const int f = n0 + col0 + j * 32 + lane;
+                    bias_w[j * 32 + lane] = f < 3 * hd ? p.bias[f] : 0.0f;
+                }
+                __syncwarp();
+            }
             // element offsets of this token's q_rot row and k/v cache row (head 0, dim 0)
             const int64_t off_q = (static_cast<int64_t>(b) * p.H * p.Nq + n) * 128;
             const int64_t off_kv = (static_cast<int64_t>(b) * p.H * rows + static_cast<int64_t>(fd.slot) * p.HW + r) * 128;
@@ -316,7 +348,7 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                     const int64_t off = type == 0 ? off_q : off_kv;
                     float bv[32];
                     if (p.bias) {
-                        const float4* b4 = reinterpret_cast<const float4*>(p.bias + f0);
+                        const float4* b4 = reinterpret_cast<const float4*>(bias_w + cchunk * 32);
 #pragma unroll
                         for (int v = 0; v < 8; ++v) {
                             const float4 t4 = b4[v];
@@ -334,7 +366,7 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                             const float2* src = pr < p.tp ? t_row + pr
                                               : pr < p.tp + p.hp ? h_col + (pr - p.tp) * p.grid_h
                                                                  : w_col + (pr - p.tp - p.hp) * p.grid_w;
-                            csv[u] = *src;           // generic load: t pairs live in the launch parameters
+                            csv[u] = *src;           // generic load: shared memory, or launch parameters and global
                         }
                     }
                     uint32_t o[16];

@@ -145,6 +145,10 @@ def _fused_reference(w, start, c, x_b, W, bias):
     ("tiny", dict(heads=3, grid_h=9, grid_w=15, window_frames=5, refresh_chunks=2, batch=2,
                   start_frames=[7, 90000]), 4, True),
     ("wan13b_480p", dict(), 2, False),
+    # cos/sin tables too large for the kernel's shared-memory copy (30 h and 30 w pairs over a
+    # 40 x 80 grid: 28.8 KB): the epilogue reads them from global memory
+    ("tiny", dict(heads=2, grid_h=40, grid_w=80, chunk_frames=1, sink_frames=1, window_frames=2,
+                  rope_t=8, rope_h=60, rope_w=60, start_frames=[11]), 3, False),
 ])
 def test_fused_qkv_rope_append_matches_fp64(name, over, chunks, attend):
     w = small_workload(WORKLOADS[name], **over)
