@@ -115,6 +115,26 @@ __device__ __forceinline__ uint4 shfl_xor_u4(uint4 v, int mask)
     return v;
 }
 
+// Tile order: the q/k feature tiles (those starting before 2*H*D) of every token tile first, then
+// the v tiles, so that the last tile of each pair -- whose epilogue nothing overlaps -- is one
+// without table reads and rotation.
+struct TileOrder {
+    int nqk, nv;                       // feature tiles per token tile: q/k (or straddling k|v), v only
+    int mtiles;
+    __device__ __forceinline__ void coords(int t, int& mt, int& nt) const
+    {
+        const int qk_tiles = mtiles * nqk;
+        if (t < qk_tiles) {
+            mt = t / nqk;
+            nt = t - mt * nqk;
+        } else {                       // only reached when nv > 0
+            const int u = t - qk_tiles;
+            mt = u / nv;
+            nt = nqk + (u - mt * nv);
+        }
+    }
+};
+
 __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_constant__ QkvRopeParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -131,7 +151,11 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
     const int pair = static_cast<int>(cluster_id_x());
     const int npairs = static_cast<int>(cluster_count_x());
     const int ntn = (3 * p.H * 128 + PBN - 1) / PBN;        // feature tiles (the last may be ragged)
-    const int ntiles = ((p.M + PBM - 1) / PBM) * ntn;
+    TileOrder order;
+    order.mtiles = (p.M + PBM - 1) / PBM;
+    order.nqk = (2 * p.H * 128 + PBN - 1) / PBN;
+    order.nv = ntn - order.nqk;
+    const int ntiles = order.mtiles * ntn;
     const int my_tiles = pair < ntiles ? (ntiles - 1 - pair) / npairs + 1 : 0;
     const int ksteps = p.C / QBK;
     const uint64_t tmo = p.timeout_ns;
@@ -169,9 +193,10 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
             bool ok = true;
             int g = 0;                                       // k-steps issued so far, over all tiles
             for (int li = 0; ok && li < my_tiles; ++li) {
-                const int tile = pair + li * npairs;
-                const int m0 = (tile / ntn) * PBM + static_cast<int>(rank) * CBM;
-                const int n0 = (tile % ntn) * PBN + static_cast<int>(rank) * CBN;
+                int mt, nt;
+                order.coords(pair + li * npairs, mt, nt);
+                const int m0 = mt * PBM + static_cast<int>(rank) * CBM;
+                const int n0 = nt * PBN + static_cast<int>(rank) * CBN;
                 for (int kk = 0; kk < ksteps; ++kk, ++g) {
                     const int st = g % QST;
                     const uint32_t ph = static_cast<uint32_t>(g / QST) & 1u;
@@ -296,9 +321,10 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                 break;
             }
             tc_fence_after();
-            const int tile = pair + li * npairs;
-            const int m0 = (tile / ntn) * PBM + static_cast<int>(rank) * CBM;
-            const int n0 = (tile % ntn) * PBN;
+            int mt, nt;
+            order.coords(pair + li * npairs, mt, nt);
+            const int m0 = mt * PBM + static_cast<int>(rank) * CBM;
+            const int n0 = nt * PBN;
             const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                   static_cast<uint32_t>(buf) * QACC_COLS + static_cast<uint32_t>(col0);
             const int m = m0 + row;
