@@ -14,27 +14,29 @@
 // half of the 192 weight rows per hidden step, and the accumulator of its 128 rows x 192
 // features lands in its own tensor memory.  Each SM stages 28 KB per hidden step of 64 instead
 // of the 40 KB a 128 x 192 tile on one SM needs, so a 6-stage ring (168 KB) keeps enough copies
-// in flight and still leaves ~60 KB of L1 for the epilogue's table reads.  4680 x 4608 makes
-// 19 x 24 = 456 pair tiles, 6 per pair on 76 pairs.  Pairs are persistent (tile t, t + pairs,
-// ...); a CTA's fp32 accumulator takes 192 of the 256 columns of a tensor-memory buffer, so two
-// tiles fit: the MMA warp fills one buffer while the epilogues of both CTAs drain the other.
-// A tile may straddle heads and the q|k|v boundaries (the epilogue finds the type and head of
-// each 32-feature chunk); rows past the last token and feature rows past 3*H*D load as zeros
-// and the epilogue skips them.
+// in flight and leaves room for the epilogue's tables.  4680 x 4608 makes 19 x 24 = 456 pair
+// tiles, 6 per pair on 76 pairs.  Pairs are persistent (tile t, t + pairs, ..., in an order
+// with the q/k tiles first and the v tiles last, so that the final tile's epilogue -- which
+// nothing overlaps -- has no table reads or rotation); a CTA's fp32 accumulator takes 192 of
+// the 256 columns of a tensor-memory buffer, so two tiles fit: the MMA warp fills one buffer
+// while the epilogues of both CTAs drain the other.  A tile may straddle heads and the q|k|v
+// boundaries (the epilogue finds the type and head of each 32-feature chunk); rows past the
+// last token and feature rows past 3*H*D load as zeros and the epilogue skips them.
 //   warp 0: TMA producer (both CTAs load into their own shared memory and count the bytes on
 //   the leader CTA's stage barrier; the leader arms it for both); warp 1: in the leader, MMA
 //   issuer (converged: every lane polls, a warp vote agrees; elect.sync issues), whose commits
 //   arrive on the barriers of both CTAs; warps 2-9: epilogue, two per TMEM lane quarter (each
 //   takes half of the columns), thread = token row, with the next 32-column TMEM load in flight
-//   while the current chunk is rotated and stored (bias read as float4), arriving on the
-//   leader's accumulator-empty barrier (sixteen warps over the pair) when a buffer is drained.
-// The epilogue is what bounds this kernel (the MMA loop alone runs at the speed of a library
+//   while the current chunk is rotated and stored, arriving (relaxed: the arrival orders no
+//   memory) on the leader's accumulator-empty barrier when a buffer is drained.
+// The epilogue is what bounded this kernel (the MMA loop alone runs at the speed of a library
 // GEMM of the same shape), and its cost is the number of distinct rows each warp instruction
-// touches: a chunk's 16 cos/sin pairs come from pair-major copies of the h and w tables, where
-// the warp's consecutive tokens read adjacent entries, each from a pointer picked by select so
-// that the 16 loads issue back to back; and the four lanes of each quad transpose their 64-byte
-// row segments with two xor-shuffle steps, so each store instruction writes 8 whole segments
-// instead of 16 bytes of 32 rows.
+// touches: the t, h and w cos/sin tables are copied into shared memory once per CTA (pair-major
+// h and w, so that the warp's consecutive tokens read adjacent entries; tables too large for
+// the area are read from global memory), a chunk's 16 pairs are loaded back to back through a
+// pointer select, each warp stages its 96 bias values per tile with coalesced loads, and the
+// four lanes of each quad transpose their 64-byte row segments with two xor-shuffle steps, so
+// each store instruction writes 8 whole segments instead of 16 bytes of 32 rows.
 // Rounding: acc (fp32, fp32 accumulation) + bias (fp32 add); q and k pairs rotated in fp32 as
 // (fmaf(x, c, -(y*s)), fmaf(x, s, y*c)); one bf16 round-to-nearest-even per output.
 #include <cuda_bf16.h>
