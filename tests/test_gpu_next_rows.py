@@ -195,10 +195,14 @@ def test_fused_qkv_rope_append_matches_fp64(name, over, chunks, attend):
                     assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (c, b, hh, err.max(), err.mean())
 
 
-def test_fused_qkv_rope_append_at_14b_shape_sampled_rows():
-    """Wan-14B 480p shape (40 heads, C = 5120, 80 feature tiles of 192, 19 token tiles of 256):
-    sampled token rows of q_rot, k and v against the fp64 projection + RoPE of those rows."""
-    w = WORKLOADS["wan14b_480p"]
+@pytest.mark.parametrize("name", ["wan14b_480p", "wan13b_720p", "stream_batch"])
+def test_fused_qkv_rope_append_at_full_shape_sampled_rows(name):
+    """Full workload shapes, sampled token rows of every stream's q_rot, k and v against the fp64
+    projection + RoPE of those rows: Wan-14B 480p (40 heads, C = 5120, 80 feature tiles of 192,
+    19 token tiles of 256); Wan-1.3B 720p (10800 tokens; its cos/sin tables, 21.5 KB, just fit
+    the kernel's shared-memory copy); the 4-stream batch (tokens of four streams in the token
+    tiles, start frames up to 1e5)."""
+    w = WORKLOADS[name]
     cfg = config(w)
     starts = list(w.start_frames)
     sess = sd.StreamSession(cfg, 1, starts, "cuda")
@@ -206,29 +210,30 @@ def test_fused_qkv_rope_append_at_14b_shape_sampled_rows():
     C = w.heads * w.head_dim
     c = 9                                           # window already wrapped: slots != frames
     x, W, bias = _proj_inputs(w, c, seed=3)
-    sd.qkv_rope_append(cfg, starts, [c], x.cuda(), W.cuda(), sess.q_rot, L.k, L.v, L.meta, sess.ws,
+    sd.qkv_rope_append(cfg, starts, [c] * w.batch, x.cuda(), W.cuda(), sess.q_rot, L.k, L.v, L.meta, sess.ws,
                        bias=bias.cuda())
     torch.cuda.synchronize()
     sd.check_device_error(sess.ws)
-    rows = np.unique(np.concatenate([np.arange(0, 4), np.linspace(0, w.nq - 1, 60).astype(np.int64),
-                                     np.arange(w.nq - 4, w.nq), np.arange(255, 258), np.arange(1559, 1562)]))
-    y = oracle.qkv_project(bits(x[0][torch.from_numpy(rows)].contiguous()), bits(W), bias.numpy())
-    t, h, ww, frame = oracle.chunk_positions(starts[0], c, w.chunk_frames, w.grid_h, w.grid_w, w.refresh_chunks)
-    rep = lambda a: np.repeat(a[rows].astype(np.float64), w.heads)
-    rot = lambda z: oracle.rope_ideal(z.reshape(-1, w.head_dim), rep(t), rep(h), rep(ww), w.rope_t, w.rope_h,
-                                      w.rope_w, w.rope_base).reshape(len(rows), w.heads, w.head_dim)
-    q, k = rot(y[:, :C]), rot(y[:, C:2 * C])
-    v = y[:, 2 * C:].reshape(len(rows), w.heads, w.head_dim)
-    qg = to_f64(sess.q_rot[0][:, torch.from_numpy(rows).cuda()])            # [H][rows][D]
-    _close(qg.transpose(1, 0, 2), q, "q_rot")
     hw = w.hw
-    meta = L.meta.cpu().numpy()[0]
-    slot_rows = []
-    for n in rows:
-        f = c * w.chunk_frames + int(n) // hw
-        s = oracle.slot_of_frame(f, w.sink_frames, w.window_frames)
-        assert tuple(meta[s]) == (f, int(t[(int(n) // hw) * hw])), (n, s, tuple(meta[s]))
-        slot_rows.append(s * hw + int(n) % hw)
-    idx = torch.tensor(slot_rows, device="cuda")
-    _close(to_f64(L.k[0][:, idx]).transpose(1, 0, 2), k, "k rows")
-    _close(to_f64(L.v[0][:, idx]).transpose(1, 0, 2), v, "v rows")
+    rows = np.unique(np.concatenate([np.arange(0, 4), np.linspace(0, w.nq - 1, 60).astype(np.int64),
+                                     np.arange(w.nq - 4, w.nq), np.arange(255, 258), np.arange(hw - 1, hw + 2)]))
+    for b in range(w.batch):
+        y = oracle.qkv_project(bits(x[b][torch.from_numpy(rows)].contiguous()), bits(W), bias.numpy())
+        t, h, ww, frame = oracle.chunk_positions(starts[b], c, w.chunk_frames, w.grid_h, w.grid_w, w.refresh_chunks)
+        rep = lambda a: np.repeat(a[rows].astype(np.float64), w.heads)
+        rot = lambda z: oracle.rope_ideal(z.reshape(-1, w.head_dim), rep(t), rep(h), rep(ww), w.rope_t, w.rope_h,
+                                          w.rope_w, w.rope_base).reshape(len(rows), w.heads, w.head_dim)
+        q, k = rot(y[:, :C]), rot(y[:, C:2 * C])
+        v = y[:, 2 * C:].reshape(len(rows), w.heads, w.head_dim)
+        qg = to_f64(sess.q_rot[b][:, torch.from_numpy(rows).cuda()])        # [H][rows][D]
+        _close(qg.transpose(1, 0, 2), q, "q_rot stream %d" % b)
+        meta = L.meta.cpu().numpy()[b]
+        slot_rows = []
+        for n in rows:
+            f = c * w.chunk_frames + int(n) // hw
+            s = oracle.slot_of_frame(f, w.sink_frames, w.window_frames)
+            assert tuple(meta[s]) == (f, int(t[(int(n) // hw) * hw])), (b, n, s, tuple(meta[s]))
+            slot_rows.append(s * hw + int(n) % hw)
+        idx = torch.tensor(slot_rows, device="cuda")
+        _close(to_f64(L.k[b][:, idx]).transpose(1, 0, 2), k, "k rows stream %d" % b)
+        _close(to_f64(L.v[b][:, idx]).transpose(1, 0, 2), v, "v rows stream %d" % b)
