@@ -10,18 +10,20 @@
 // the frames' cache slots, without a round trip of q, k, v through memory.
 //
 // Tiling: clusters of two CTAs on the two SMs of a TPC share each MMA (tcgen05.mma.cta_group::2,
-// M = 256): a pair tile is 256 tokens x 192 features; each CTA holds its 128 token rows and
-// half of the 192 weight rows per hidden step, and the accumulator of its 128 rows x 192
-// features lands in its own tensor memory.  Each SM stages 28 KB per hidden step of 64 instead
-// of the 40 KB a 128 x 192 tile on one SM needs, so a 6-stage ring (168 KB) keeps enough copies
-// in flight and leaves room for the epilogue's tables.  4680 x 4608 makes 19 x 24 = 456 pair
-// tiles, 6 per pair on 76 pairs.  Pairs are persistent (tile t, t + pairs, ..., in an order
-// with the q/k tiles first and the v tiles last, so that the final tile's epilogue -- which
-// nothing overlaps -- has no table reads or rotation); a CTA's fp32 accumulator takes 192 of
-// the 256 columns of a tensor-memory buffer, so two tiles fit: the MMA warp fills one buffer
-// while the epilogues of both CTAs drain the other.  A tile may straddle heads and the q|k|v
-// boundaries (the epilogue finds the type and head of each 32-feature chunk); rows past the
-// last token and feature rows past 3*H*D load as zeros and the epilogue skips them.
+// M = 256): a pair tile is 256 tokens x 256 features; each CTA holds its 128 token rows and
+// half of the 256 weight rows per hidden step, and the accumulator of its 128 rows x 256
+// features lands in its own tensor memory.  Each SM stages 32 KB per hidden step of 64 (a
+// 128 x 256 tile on one SM would need 48 KB) and spends 512 MMA cycles on it, more than the
+// step's copies and barrier handshake cost; a 6-stage ring (192 KB) keeps enough copies in
+// flight next to the epilogue's tables.  4680 x 4608 makes 19 x 18 = 342 pair tiles (4.5 per
+// pair on 76 pairs), 4680 x 15360 (14B) 19 x 60 = 1140 (15 per pair).  Pairs are persistent
+// (tile t, t + pairs, ..., in an order with the q/k tiles first and the v tiles last, so that
+// the final tile's epilogue -- which nothing overlaps -- has no table reads or rotation); a
+// CTA's fp32 accumulator fills a 256-column buffer of tensor memory, so two tiles fit: the MMA
+// warp fills one buffer while the epilogues of both CTAs drain the other.  A tile may straddle
+// heads and the q|k|v boundaries (the epilogue finds the type and head of each 32-feature
+// chunk); rows past the last token and feature rows past 3*H*D (odd head counts) load as zeros
+// and the epilogue skips them.
 //   warp 0: TMA producer (both CTAs load into their own shared memory and count the bytes on
 //   the leader CTA's stage barrier; the leader arms it for both); warp 1: in the leader, MMA
 //   issuer (converged: every lane polls, a warp vote agrees; elect.sync issues), whose commits
@@ -34,7 +36,7 @@
 // touches: the t, h and w cos/sin tables are copied into shared memory once per CTA (pair-major
 // h and w, so that the warp's consecutive tokens read adjacent entries; tables too large for
 // the area are read from global memory), a chunk's 16 pairs are loaded back to back through a
-// pointer select, each warp stages its 96 bias values per tile with coalesced loads, and the
+// pointer select, each warp stages its 128 bias values per tile with coalesced loads, and the
 // four lanes of each quad transpose their 64-byte row segments with two xor-shuffle steps, so
 // each store instruction writes 8 whole segments instead of 16 bytes of 32 rows.
 // Rounding: acc (fp32, fp32 accumulation) + bias (fp32 add); q and k pairs rotated in fp32 as
@@ -52,15 +54,18 @@ namespace sdv2 {
 namespace {
 
 constexpr int PBM = 256;                       // tokens per pair tile
-constexpr int PBN = 192;                       // features per pair tile
+constexpr int PBN = 256;                       // features per pair tile
 constexpr int CBM = PBM / 2;                   // token rows in each CTA
 constexpr int CBN = PBN / 2;                   // weight rows in each CTA
 static_assert(PBN % 64 == 0 && PBN <= 256, "N of an M = 256 pair MMA; the epilogue splits it in 32-column chunks per half");
-constexpr int QBK = 64;                        // hidden elements per step (128 bytes of bf16)
+constexpr int QBK = 64;                        // hidden elements per TMA box (128 bytes of bf16)
+constexpr int KSUB = 1;                        // boxes of QBK per ring stage (one barrier handshake)
 constexpr int QST = 6;                         // ring stages
 constexpr uint32_t A_BYTES = CBM * QBK * 2;    // 16 KB
-constexpr uint32_t B_BYTES = CBN * QBK * 2;    // 12 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t B_BYTES = CBN * QBK * 2;    // 16 KB
+constexpr uint32_t SUB_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t STAGE_BYTES = KSUB * SUB_BYTES;
+static_assert(128 % (QBK * KSUB) == 0, "the hidden dimension (heads x 128) is a whole number of ring stages");
 constexpr int QTHREADS = 10 * 32;
 constexpr int QEPI_WARPS = 8;
 constexpr uint32_t QACC_COLS = 256;            // accumulator buffer stride
@@ -159,7 +164,7 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
     order.nv = ntn - order.nqk;
     const int ntiles = order.mtiles * ntn;
     const int my_tiles = pair < ntiles ? (ntiles - 1 - pair) / npairs + 1 : 0;
-    const int ksteps = p.C / QBK;
+    const int ksteps = p.C / (QBK * KSUB);
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -212,8 +217,11 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                     const uint32_t sa = s0 + st * STAGE_BYTES;
                     if (rank == 0) mbar_arrive_expect_tx(QBAR(QB_FULL + st), 2 * STAGE_BYTES);
                     const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(st);
-                    tma_load_3d_pair(sa, &p.xmap, fb, kk * QBK, m0, 0);
-                    tma_load_3d_pair(sa + A_BYTES, &p.wmap, fb, kk * QBK, n0, 0);
+#pragma unroll
+                    for (int sb = 0; sb < KSUB; ++sb) {
+                        tma_load_3d_pair(sa + sb * SUB_BYTES, &p.xmap, fb, (kk * KSUB + sb) * QBK, m0, 0);
+                        tma_load_3d_pair(sa + sb * SUB_BYTES + A_BYTES, &p.wmap, fb, (kk * KSUB + sb) * QBK, n0, 0);
+                    }
                     pend |= 1u << st;
                     par = (par & ~(1u << st)) | (ph << st);
                 }
@@ -261,9 +269,10 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
                     const uint64_t a = dA + static_cast<uint64_t>(st) * kStage;
                     const uint64_t b = dB + static_cast<uint64_t>(st) * kStage;
 #pragma unroll
-                    for (int k = 0; k < QBK / 16; ++k)
-                        mma_ss_pair_warp(dacc, a + static_cast<uint64_t>(k * 2), b + static_cast<uint64_t>(k * 2), idesc,
-                                         (kk > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < KSUB * (QBK / 16); ++k) {
+                        const uint64_t off = static_cast<uint64_t>((k / (QBK / 16)) * (SUB_BYTES >> 4) + (k % (QBK / 16)) * 2);
+                        mma_ss_pair_warp(dacc, a + off, b + off, idesc, (kk > 0 || k > 0) ? 1u : 0u);
+                    }
                     mma_commit_pair_warp(QBAR(QB_EMPTY + st), kBothCtas);
                 }
                 if (!ok) break;

@@ -40,7 +40,7 @@ def main():
     ap.add_argument("--peak-gbs", type=float, default=0.0, help="HBM peak (GB/s); default: MEASURED_PEAKS.json or 6800")
     ap.add_argument("--layers", type=int, default=8, help="distinct layer caches cycled (more than L2 in total)")
     ap.add_argument("--only", default="", help="comma-separated subset of: append, attention, rerotate, sink, "
-                    "qkv, cublas, unfused, motion, noise, copies (default: all)")
+                    "qkv, cublas, unfused, qkv14b, motion, noise, copies (default: all)")
     args = ap.parse_args()
     only = {x.strip() for x in args.only.split(",") if x.strip()}
 
@@ -163,6 +163,34 @@ def main():
                ms=_time(unfused, 60, stream))
     del sess, qkv
     torch.cuda.empty_cache()
+
+    # fused projection at the Wan-14B 480p shape (C = 5120, 40 heads: 80 feature tiles, a
+    # 5120-long hidden dimension) against the library GEMM of the same shape
+    if want("qkv14b"):
+        w14 = WORKLOADS["wan14b_480p"]
+        cfg14 = sd.StreamConfig.make(**stream_config_dict(w14))
+        nl14 = max(1, min(nl, 4))
+        sess14 = StreamSession(cfg14, nl14, w14.start_frames, dev, stream)
+        C14 = w14.heads * w14.head_dim
+        xs14 = [torch.randn((1, w14.nq, C14), generator=g, device=dev).to(torch.bfloat16) for _ in range(nl14)]
+        W14 = (torch.randn((3 * C14, C14), generator=g, device=dev) / C14 ** 0.5).to(torch.bfloat16)
+        b14 = torch.randn(3 * C14, generator=g, device=dev).float() * 0.1
+        flops14 = 2.0 * w14.nq * 3 * C14 * C14
+
+        def fused14(i):
+            L = sess14.layers[i % nl14]
+            sd.qkv_rope_append(cfg14, w14.start_frames, [steady], xs14[i % nl14], W14, sess14.q_rot, L.k, L.v, L.meta,
+                               sess14.ws, bias=b14, stream=stream)
+        report("sdv2_qkv_rope_append", w14.name + " (x [4680][5120] @ W[15360][5120]^T + bias, RoPE, append)",
+               flops_per_call=flops14, ms=_time(fused14, 30, stream))
+        y14 = torch.empty((1, w14.nq, 3 * C14), dtype=torch.bfloat16, device=dev)
+
+        def gemm14(i):
+            torch.matmul(xs14[i % nl14][0], W14.t(), out=y14[0])
+        report("projection GEMM alone: torch.matmul (cuBLAS), bf16 out, no bias or RoPE", w14.name,
+               flops_per_call=flops14, ms=_time(gemm14, 30, stream))
+        del sess14, xs14, W14, y14
+        torch.cuda.empty_cache()
 
     # size-matched reference: a plain device-to-device copy (torch copy_) moving the same bytes
     # (half read, half written) as each HBM-bound call, over 8 buffer pairs cycled so that the
