@@ -164,6 +164,7 @@ struct QkvRopeParams {
     uint64_t timeout_ns;
     int32_t M, C, B, H, HW, grid_h, grid_w, F, nslots, Nq;
     int32_t tp, hp, wp;
+    int32_t m_fastest;                        // tile order: token tiles fastest (weights larger than L2)
     FrameDesc frames[kMaxChunkFrames];
     float2 tcs[kMaxTimePairs];
 };

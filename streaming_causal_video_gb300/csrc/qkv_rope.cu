@@ -124,21 +124,29 @@ __device__ __forceinline__ uint4 shfl_xor_u4(uint4 v, int mask)
 
 // Tile order: the q/k feature tiles (those starting before 2*H*D) of every token tile first, then
 // the v tiles, so that the last tile of each pair -- whose epilogue nothing overlaps -- is one
-// without table reads and rotation.
+// without table reads and rotation.  Within each part the feature tiles vary fastest, unless the
+// weights do not fit in L2 (m_fastest): then the token tiles vary fastest, so that the pairs of a
+// wave share a few weight slices and the token rows stay in L2 from wave to wave instead of the
+// whole weight matrix streaming from DRAM once per wave.
 struct TileOrder {
     int nqk, nv;                       // feature tiles per token tile: q/k (or straddling k|v), v only
     int mtiles;
+    bool m_fastest;
     __device__ __forceinline__ void coords(int t, int& mt, int& nt) const
     {
         const int qk_tiles = mtiles * nqk;
-        if (t < qk_tiles) {
-            mt = t / nqk;
-            nt = t - mt * nqk;
-        } else {                       // only reached when nv > 0
-            const int u = t - qk_tiles;
-            mt = u / nv;
-            nt = nqk + (u - mt * nv);
+        const bool qk = t < qk_tiles;
+        const int u = qk ? t : t - qk_tiles;   // the v part is only reached when nv > 0
+        const int per = qk ? nqk : nv;         // feature tiles of this part
+        if (m_fastest) {
+            const int j = u / mtiles;
+            mt = u - j * mtiles;
+            nt = j;
+        } else {
+            mt = u / per;
+            nt = u - mt * per;
         }
+        if (!qk) nt += nqk;
     }
 };
 
@@ -162,6 +170,7 @@ __global__ void __launch_bounds__(QTHREADS, 1) qkv_rope_kernel(const __grid_cons
     order.mtiles = (p.M + PBM - 1) / PBM;
     order.nqk = (2 * p.H * 128 + PBN - 1) / PBN;
     order.nv = ntn - order.nqk;
+    order.m_fastest = p.m_fastest != 0;
     const int ntiles = order.mtiles * ntn;
     const int my_tiles = pair < ntiles ? (ntiles - 1 - pair) / npairs + 1 : 0;
     const int ksteps = p.C / (QBK * KSUB);
@@ -550,6 +559,9 @@ cudaError_t launch_qkv_rope(QkvRopeParams& p, const void* x, const void* w, int6
         }
         slot.store(pairs_max);
     }
+    int l2_bytes = 0;
+    cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev);
+    p.m_fastest = 3LL * p.H * 128 * p.C * 2 > static_cast<int64_t>(l2_bytes) / 2 ? 1 : 0;
     const int64_t ntiles = static_cast<int64_t>((p.M + PBM - 1) / PBM) * ((3 * p.H * 128 + PBN - 1) / PBN);
     const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(ntiles, pairs_max));
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
