@@ -84,9 +84,28 @@ def test_guard_bands_stay_untouched():
         if c % 4 == 0 and c > 0:
             sd.rope_refresh_rerotate(cfg, [c, c], bufs["k"][1], meta)
             sd.sink_update(cfg, [c, c], [1, 1], bufs["k"][1], bufs["v"][1], meta)
+    # the fused projection (reads x, W and bias; writes q_rot, the chunk's cache rows and meta),
+    # the allocation-free attention (writes out and lse) and the noise controller (rate, state)
+    C = H * D
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x_b, x, xp = _guarded((B, nq, C), torch.bfloat16, 0.5)
+    x.copy_(torch.randn((B, nq, C), generator=g, device="cuda").to(torch.bfloat16))
+    wq_b, wq, wqp = _guarded((3 * C, C), torch.bfloat16, -0.25)
+    wq.copy_((torch.randn((3 * C, C), generator=g, device="cuda") / C ** 0.5).to(torch.bfloat16))
+    bias_b, bias, bp = _guarded((3 * C,), torch.float32, 1.5)
+    bias.copy_(torch.randn(3 * C, generator=g, device="cuda") * 0.1)
+    sd.qkv_rope_append(cfg, W.start_frames, [6, 6], x, wq, bufs["q_rot"][1], bufs["k"][1], bufs["v"][1], meta, ws,
+                       bias=bias)
+    sd.chunk_attention_noalloc(cfg, [6, 6], bufs["q_rot"][1], bufs["k"][1], bufs["v"][1], bufs["out"][1], lse=lse)
     sd.motion_l2(frames, ssd, m)
+    rate_b, rate, rp = _guarded((2, 4), torch.float32, -2.0)
+    state_b, state, stp = _guarded((2,), torch.float32, 9.0)
+    state.fill_(-1.0)
+    ctl = sd.NoiseCtl(motion_lo=1.0, motion_hi=80.0, rate_lo=0.2, rate_hi=0.9, ema=0.5, more_noise_when_fast=1)
+    sd.noise_from_motion(ctl, m, rate, state)
     torch.cuda.synchronize()
     sd.check_device_error(ws)
+    sd.noalloc_check_device_error()
 
     def bands_ok(base, pad, fill):
         h = base.cpu()
@@ -100,6 +119,11 @@ def test_guard_bands_stay_untouched():
     assert bands_ok(ssd_b, sp, 0x77)
     assert bands_ok(m_b, mp2, 3.5)
     assert bands_ok(frames_b, fp_, 0x33)
+    assert bands_ok(x_b, xp, 0.5)
+    assert bands_ok(wq_b, wqp, -0.25)
+    assert bands_ok(bias_b, bp, 1.5)
+    assert bands_ok(rate_b, rp, -2.0)
+    assert bands_ok(state_b, stp, 9.0)
 
 
 def test_cuda_graph_replay_equals_eager():
