@@ -151,6 +151,35 @@ def test_cuda_graph_replay_equals_eager():
     np.testing.assert_array_equal(bits(graphed.out), bits(eager.out))
 
 
+def test_cuda_graph_replay_of_fused_projection_equals_eager():
+    """The fused projection is launched as clusters of two CTAs (its first call on a device also
+    sets the shared-memory limit and reads how many pairs fit); captured, as its first call in
+    the process or not, it replays to exactly what the eager call writes."""
+    cfg = config(W)
+    C = W.heads * 128
+    g = torch.Generator(device="cuda").manual_seed(12)
+    x = torch.randn((W.batch, W.nq, C), generator=g, device="cuda").to(torch.bfloat16)
+    wq = (torch.randn((3 * C, C), generator=g, device="cuda") / C ** 0.5).to(torch.bfloat16)
+    bias = torch.randn(3 * C, generator=g, device="cuda") * 0.1
+    eager = sd.StreamSession(cfg, 1, W.start_frames, "cuda")
+    graphed = sd.StreamSession(cfg, 1, W.start_frames, "cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        L = graphed.layers[0]
+        sd.qkv_rope_append(cfg, W.start_frames, [2, 2], x, wq, graphed.q_rot, L.k, L.v, L.meta, graphed.ws,
+                           bias=bias, stream=s)
+    graph.replay()
+    L = eager.layers[0]
+    sd.qkv_rope_append(cfg, W.start_frames, [2, 2], x, wq, eager.q_rot, L.k, L.v, L.meta, eager.ws, bias=bias)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(graphed.q_rot), bits(eager.q_rot))
+    np.testing.assert_array_equal(bits(graphed.layers[0].k), bits(eager.layers[0].k))
+    np.testing.assert_array_equal(bits(graphed.layers[0].v), bits(eager.layers[0].v))
+    np.testing.assert_array_equal(graphed.layers[0].meta.cpu().numpy(), eager.layers[0].meta.cpu().numpy())
+
+
 def test_two_sessions_on_two_streams_equal_serial_runs():
     """Two independent sessions (different configurations, one of them large enough to use key
     splits) stepped concurrently on two CUDA streams give, bit for bit, what each gives when run
