@@ -129,7 +129,8 @@ __device__ __forceinline__ uint4 shfl_xor_u4(uint4 v, int mask)
 // wave share a few weight slices and the token rows stay in L2 from wave to wave instead of the
 // whole weight matrix streaming from DRAM once per wave.
 struct TileOrder {
-    int nqk, nv;                       // feature tiles per token tile: q/k (or straddling k|v), v only
+    int nqk, nv;                       // feature tiles per token tile: q/k (2*H*D is a multiple of
+                                       // 256), v (the last one ragged for odd H)
     int mtiles;
     bool m_fastest;
     __device__ __forceinline__ void coords(int t, int& mt, int& nt) const
