@@ -218,6 +218,47 @@ def test_two_sessions_on_two_streams_equal_serial_runs():
         np.testing.assert_array_equal(cb[c], sb_[c], err_msg="session b, chunk %d" % c)
 
 
+def test_fused_projections_on_two_streams_equal_serial_runs():
+    """Two fused projections (persistent CTA-pair grids sized to the whole GPU) issued on two
+    streams at once -- at the 1.3B-480p shape and at a small one -- write, bit for bit, what each
+    writes alone: pairs that cannot be resident together run later, nothing waits across grids."""
+    shapes = [WORKLOADS["wan13b_480p"], W]
+    sessions = {}
+
+    def inputs(w, seed):
+        C = w.heads * 128
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        x = torch.randn((w.batch, w.nq, C), generator=g, device="cuda").to(torch.bfloat16)
+        wq = (torch.randn((3 * C, C), generator=g, device="cuda") / C ** 0.5).to(torch.bfloat16)
+        return x, wq, torch.randn(3 * C, generator=g, device="cuda") * 0.1
+    ins = [inputs(w, 30 + i) for i, w in enumerate(shapes)]
+
+    def run(concurrent):
+        streams = [torch.cuda.Stream(), None]
+        streams[1] = torch.cuda.Stream() if concurrent else streams[0]
+        outs = []
+        for i, w in enumerate(shapes):
+            sessions[i] = sd.StreamSession(config(w), 1, list(w.start_frames), "cuda")
+        torch.cuda.synchronize()
+        for rep in range(20):
+            for i, w in enumerate(shapes):
+                S, L = sessions[i], sessions[i].layers[0]
+                x, wq, bias = ins[i]
+                sd.qkv_rope_append(config(w), list(w.start_frames), [5] * w.batch, x, wq, S.q_rot, L.k, L.v, L.meta,
+                                   S.ws, bias=bias, stream=streams[i])
+        torch.cuda.synchronize()
+        for i in range(len(shapes)):
+            sd.check_device_error(sessions[i].ws)
+            outs.append((bits(sessions[i].q_rot).copy(), bits(sessions[i].layers[0].k).copy()))
+        return outs
+
+    conc = run(True)
+    ser = run(False)
+    for i in range(len(shapes)):
+        np.testing.assert_array_equal(conc[i][0], ser[i][0])
+        np.testing.assert_array_equal(conc[i][1], ser[i][1])
+
+
 def test_undersized_or_offset_buffers_are_refused_on_the_host():
     """A buffer whose storage ends before the bytes a call touches raises ValueError in the
     binding; nothing is launched (the error word stays clear and a correct call follows)."""
